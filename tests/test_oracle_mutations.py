@@ -1,0 +1,134 @@
+"""Planted mistakes in the oracle (on the CPU) must be caught by the pins.
+
+Each test swaps one oracle function for a subtly wrong copy and checks that a
+pin from tests/test_oracle_pins.py now fails.  This is how we know the pins
+would notice a dropped term, a wrong sign or index, or a transposed operand.
+"""
+import math
+
+import numpy as np
+import pytest
+
+from oracle import mapflow_oracle as orc
+from tests import test_oracle_pins as pins
+
+
+def _attention_rows_factory(scale_fn=None, causal_strict=False, sign=1.0):
+    def attention_rows(q_rows, k_seq, row_pos, causal):
+        d = q_rows.shape[1]
+        L = k_seq.shape[0]
+        S = sign * (q_rows @ k_seq.T) / (scale_fn(d) if scale_fn else math.sqrt(d))
+        if causal:
+            if causal_strict:
+                allowed = np.arange(L)[None, :] < row_pos[:, None]
+                allowed[:, 0] = True
+            else:
+                allowed = np.arange(L)[None, :] <= row_pos[:, None]
+        else:
+            allowed = np.ones((len(row_pos), L), dtype=bool)
+        S = np.where(allowed, S, -np.inf)
+        m = S.max(axis=1)
+        E = np.exp(S - m[:, None])
+        l = E.sum(axis=1)
+        return E / l[:, None], m, l
+    return attention_rows
+
+
+@pytest.mark.parametrize("mut", [
+    dict(scale_fn=lambda d: 1.0),            # dropped 1/sqrt(d)
+    dict(scale_fn=lambda d: float(d)),       # 1/d instead of 1/sqrt(d)
+    dict(causal_strict=True),                # mask excludes the diagonal
+    dict(sign=-1.0),                         # sign flip of the logits
+])
+def test_sdpa_pin_catches_softmax_mistakes(monkeypatch, mut):
+    monkeypatch.setattr(orc, "attention_rows", _attention_rows_factory(**mut))
+    assert pins.check_sdpa_closed_form(o=orc) > 1e-3
+
+
+def test_onehot_pin_catches_transposed_head_map(monkeypatch):
+    real = orc.retrieve_rows
+
+    def transposed(P, W, v, H_kv):
+        # plausible mistake: contract W over its first index
+        Wt = np.zeros_like(W)
+        n = min(W.shape)
+        Wt[:n, :n] = W[:n, :n].T
+        return real(P, Wt, v, H_kv)
+    monkeypatch.setattr(orc, "retrieve_rows", transposed)
+    assert pins.check_onehot_head_map(o=orc) > 1e-3
+
+
+def test_onehot_pin_catches_wrong_gqa_grouping(monkeypatch):
+    def wrong_group(P_kept_rows, W, v_seq, H_kv):
+        Hs, n, L = P_kept_rows.shape
+        Hr = W.shape[0]
+        A_hat = np.tensordot(W, P_kept_rows, axes=([1], [0]))
+        out = np.zeros((n, Hr, v_seq.shape[2]))
+        for i in range(Hr):
+            out[:, i, :] = A_hat[i] @ v_seq[:, i % H_kv, :]  # interleaved, not contiguous
+        return out
+    monkeypatch.setattr(orc, "retrieve_rows", wrong_group)
+    assert pins.check_onehot_head_map(o=orc) > 1e-3
+
+
+def test_no_renorm_pin_catches_renormalisation(monkeypatch):
+    real = orc.kept_mask_rows
+
+    def renorm_mask(grid, kept, bi, s, n_rows):
+        mk = real(grid, kept, bi, s, n_rows)
+        return mk * 1.05  # e.g. dividing by the kept fraction
+    monkeypatch.setattr(orc, "kept_mask_rows", renorm_mask)
+    assert pins.check_no_renormalisation(o=orc) > 1e-3
+
+
+def _select_factory(tie_high=False, strict=False, frac_bits=20):
+    def select_topp(mass, p):
+        mass = np.asarray(mass, dtype=np.float64)
+        n = len(mass)
+        key = (lambda b: (-mass[b], -b)) if tie_high else (lambda b: (-mass[b], b))
+        order = sorted(range(n), key=key)
+        q = [int(np.rint(mass[b] * 2.0 ** 32)) for b in range(n)]
+        tot = sum(q)
+        pq = int(np.rint(p * 2 ** frac_bits))
+        acc, k = 0, 0
+        while k < n and ((acc << frac_bits) <= pq * tot if strict else (acc << frac_bits) < pq * tot):
+            acc += q[order[k]]
+            k += 1
+        return sorted(order[:k])
+    return select_topp
+
+
+@pytest.mark.parametrize("mut", [dict(tie_high=True), dict(strict=True)])
+def test_bruteforce_pin_catches_selection_mistakes(mut):
+    bad = _select_factory(**mut)
+    caught = False
+    for seed in range(40):
+        rng = np.random.default_rng(seed)
+        n = int(rng.integers(2, 9))
+        mass = rng.random(n)
+        mass[1] = mass[0]
+        mass[-1] = mass[0]
+        mass = mass.astype(np.float32).astype(np.float64)
+        for p in (0.5, 0.8, 0.95, 1.0):
+            kept = bad(mass, p)
+            size, subsets = pins.selection_bruteforce(mass, p)
+            dropped = [b for b in range(n) if b not in kept]
+            ok = len(kept) == size and tuple(kept) in subsets and all(
+                mass[a] > mass[b] or (mass[a] == mass[b] and a < b)
+                for a in kept for b in dropped)
+            caught |= not ok
+    assert caught
+
+
+def test_mass_pin_catches_block_offset(monkeypatch):
+    """Summing the wrong column range (off by one block edge) is caught by the
+    uniform-attention closed form."""
+    def off_by_one(P_rows, B, n_cand):
+        L = P_rows.shape[1]
+        out = np.zeros(n_cand)
+        for bj in range(n_cand):
+            out[bj] = P_rows[:, bj * B:min(L, (bj + 1) * B + 1)].sum()
+        return out
+    monkeypatch.setattr(orc, "block_masses", off_by_one)
+    with pytest.raises(AssertionError):
+        pins.test_uniform_causal_closed_form(64, 8)
