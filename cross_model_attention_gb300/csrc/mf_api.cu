@@ -1,0 +1,547 @@
+// mf_api.cu — the C ABI of libmapflow (declared in include/mapflow.h):
+// argument validation, the per-handle block grid, device buffers, TMA
+// tensor maps, and the launch sequence of the compressor and the retrieval.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/mapflow.h"
+#include "mf_internal.cuh"
+
+using namespace mf;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(MF_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define MF_CUDA(call, what)                     \
+  do {                                          \
+    cudaError_t e_ = (call);                    \
+    if (e_ != cudaSuccess) return cuda_fail(e_, what); \
+  } while (0)
+
+// ------------------------------------------------------------ tensor maps --
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 map: `inner` elements per row, `rows` rows, `stride` bytes between
+// rows; box = box_inner x box_rows; 128-byte swizzle; out-of-range reads give 0.
+int make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t stride,
+             uint32_t box_inner, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return fail(MF_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable (driver too old?)");
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {stride};
+  cuuint32_t box[2] = {box_inner, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MF_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return MF_OK;
+}
+
+}  // namespace
+
+// --------------------------------------------------------------- handle --
+struct LayerState {
+  bool valid = false;
+  int dtype = -1;
+  int d = 0;
+  float p = 0.f;
+  long long nnz = 0;
+  void* meta = nullptr;    // one allocation carved into the arrays below
+  size_t meta_bytes = 0;
+  float* mass = nullptr;
+  float* row_max = nullptr;
+  float* row_sum = nullptr;
+  int* kcount = nullptr;
+  int* keptcols = nullptr;
+  int* row_ptr = nullptr;
+  int* tile_of = nullptr;
+  int* union_cnt = nullptr;
+  int* union_list = nullptr;
+  long long* nnz_dev = nullptr;
+  int* col_idx = nullptr;
+  uint16_t* values = nullptr;
+  size_t values_bytes = 0, colidx_bytes = 0;
+  CUtensorMap pmap;  // values as [nnz*B rows][B cols], 64x64 boxes (retrieval)
+};
+
+struct mf_bsr_s {
+  int n_layers = 0, T = 0, H_s = 0, B = 0, causal = 1, n_seqs = 0;
+  int R = 0, C = 0, n_tiles = 0, n_slabs = 0;
+  std::vector<int> cu;
+  std::vector<RowBlock> rbs;
+  std::vector<RowTile> tiles;
+  std::vector<RowSlab> slabs;
+  RowBlock* rbs_d = nullptr;
+  RowTile* tiles_d = nullptr;
+  RowSlab* slabs_d = nullptr;
+  int* err_d = nullptr;
+  long long* host_pinned = nullptr;  // [0] nnz, [1] error word
+  mf_alloc_fn alloc = nullptr;
+  mf_free_fn dealloc = nullptr;
+  void* ctx = nullptr;
+  std::vector<LayerState> layers;
+};
+
+namespace {
+
+void* dev_alloc(mf_bsr_t h, size_t bytes, cudaStream_t s) {
+  if (bytes == 0) bytes = 256;
+  if (h->alloc) return h->alloc(bytes, h->ctx, s);
+  void* p = nullptr;
+  if (cudaMallocAsync(&p, bytes, s) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return p;
+}
+
+void dev_free(mf_bsr_t h, void* p, cudaStream_t s) {
+  if (!p) return;
+  if (h->dealloc) h->dealloc(p, h->ctx, s);
+  else cudaFreeAsync(p, s);
+}
+
+void release_layer(mf_bsr_t h, LayerState& L, cudaStream_t s) {
+  dev_free(h, L.meta, s);
+  dev_free(h, L.values, s);
+  dev_free(h, L.col_idx, s);
+  L = LayerState();
+}
+
+size_t align_up(size_t x) { return (x + 255) & ~size_t(255); }
+
+int check_shapes(int dtype, int d, int B) {
+  if (B != 64 && B != 128) return 0;
+  if (d != 64 && d != 128) return 0;
+  if (dtype == MF_DTYPE_BF16) return 1;
+  if (dtype == MF_DTYPE_F32) return !(d == 128 && B == 128);
+  return 0;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mf_version(void) { return 100; }
+
+const char* mf_last_error(void) { return g_last_error.c_str(); }
+
+int mf_supported(int dtype, int d, int B) { return check_shapes(dtype, d, B); }
+
+int mf_bsr_create(mf_bsr_t* out, int n_layers, int T, int H_s, int B, int causal,
+                  const int32_t* cu_seqlens_host, int n_seqs, mf_alloc_fn alloc_fn,
+                  mf_free_fn free_fn, void* alloc_ctx) {
+  if (!out) return fail(MF_ERR_ARG, "out is NULL");
+  *out = nullptr;
+  if (n_layers < 1 || T < 1 || H_s < 1 || n_seqs < 1 || !cu_seqlens_host)
+    return fail(MF_ERR_ARG, "n_layers, T, H_s, n_seqs must be >= 1 and cu_seqlens non-NULL");
+  if ((alloc_fn == nullptr) != (free_fn == nullptr))
+    return fail(MF_ERR_ARG, "alloc_fn and free_fn must both be set or both be NULL");
+  if (B != 64 && B != 128) return fail(MF_ERR_UNSUPPORTED, "block size %d (supported: 64, 128)", B);
+  if (H_s > 128) return fail(MF_ERR_UNSUPPORTED, "H_s = %d > 128", H_s);
+  if (causal != 0 && causal != 1) return fail(MF_ERR_ARG, "causal must be 0 or 1");
+  if (cu_seqlens_host[0] != 0) return fail(MF_ERR_ARG, "cu_seqlens[0] must be 0");
+  for (int s = 0; s < n_seqs; ++s) {
+    const int L = cu_seqlens_host[s + 1] - cu_seqlens_host[s];
+    if (L < 0) return fail(MF_ERR_ARG, "cu_seqlens must be non-decreasing (sequence %d)", s);
+    if (L > 256 * B)
+      return fail(MF_ERR_UNSUPPORTED, "sequence %d has length %d > 256*B = %d", s, L, 256 * B);
+  }
+  if (cu_seqlens_host[n_seqs] != T)
+    return fail(MF_ERR_ARG, "cu_seqlens[n_seqs] = %d != T = %d", cu_seqlens_host[n_seqs], T);
+
+  mf_bsr_t h = new mf_bsr_s();
+  h->n_layers = n_layers;
+  h->T = T;
+  h->H_s = H_s;
+  h->B = B;
+  h->causal = causal;
+  h->n_seqs = n_seqs;
+  h->alloc = alloc_fn;
+  h->dealloc = free_fn;
+  h->ctx = alloc_ctx;
+  h->cu.assign(cu_seqlens_host, cu_seqlens_host + n_seqs + 1);
+  long long cand = 0;
+  for (int s = 0; s < n_seqs; ++s) {
+    const int start = h->cu[s], L = h->cu[s + 1] - h->cu[s];
+    const int nb = (L + B - 1) / B;
+    const int rb_first = (int)h->rbs.size();
+    for (int bi = 0; bi < nb; ++bi) {
+      h->rbs.push_back(RowBlock{start, L, bi, (int)cand});
+      cand += causal ? bi + 1 : nb;
+      for (int half = 0; half < B / 64; ++half)
+        if (bi * B + half * 64 < L) h->slabs.push_back(RowSlab{rb_first + bi, half});
+    }
+    const int nt = (L + 127) / 128;
+    for (int tl = 0; tl < nt; ++tl) h->tiles.push_back(RowTile{start, L, tl, rb_first + tl * (128 / B)});
+  }
+  if (cand > (1ll << 30)) {
+    delete h;
+    return fail(MF_ERR_UNSUPPORTED, "too many candidate blocks");
+  }
+  // heaviest tiles first: causal work grows with the tile index
+  std::stable_sort(h->tiles.begin(), h->tiles.end(),
+                   [&](const RowTile& a, const RowTile& b) {
+                     const int wa = causal ? a.tl : 0, wb = causal ? b.tl : 0;
+                     return wa > wb;
+                   });
+  h->R = (int)h->rbs.size();
+  h->C = (int)cand;
+  h->n_tiles = (int)h->tiles.size();
+  h->n_slabs = (int)h->slabs.size();
+  h->layers.resize(n_layers);
+
+  auto put = [&](void** dst, const void* src, size_t bytes) -> int {
+    void* p = dev_alloc(h, bytes, nullptr);
+    if (!p) return fail(MF_ERR_OOM, "allocation of %zu bytes failed", bytes);
+    *dst = p;
+    if (src) {
+      cudaError_t e = cudaMemcpy(p, src, bytes, cudaMemcpyHostToDevice);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(tables)");
+    }
+    return MF_OK;
+  };
+  int rc = put((void**)&h->rbs_d, h->rbs.data(), sizeof(RowBlock) * h->rbs.size());
+  if (rc == MF_OK) rc = put((void**)&h->tiles_d, h->tiles.data(), sizeof(RowTile) * h->tiles.size());
+  if (rc == MF_OK) rc = put((void**)&h->slabs_d, h->slabs.data(), sizeof(RowSlab) * h->slabs.size());
+  if (rc == MF_OK) rc = put((void**)&h->err_d, nullptr, sizeof(int));
+  if (rc == MF_OK) {
+    cudaError_t e = cudaMemset(h->err_d, 0, sizeof(int));
+    if (e == cudaSuccess) e = cudaMallocHost((void**)&h->host_pinned, 2 * sizeof(long long));
+    if (e != cudaSuccess) rc = cuda_fail(e, "handle setup");
+  }
+  if (rc == MF_OK) {
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) rc = cuda_fail(e, "handle setup sync");
+  }
+  if (rc != MF_OK) {
+    std::string msg = g_last_error;
+    mf_bsr_destroy(h);
+    g_last_error = msg;
+    return rc;
+  }
+  *out = h;
+  return MF_OK;
+}
+
+void mf_bsr_destroy(mf_bsr_t h) {
+  if (!h) return;
+  cudaDeviceSynchronize();
+  for (auto& L : h->layers) release_layer(h, L, nullptr);
+  dev_free(h, h->rbs_d, nullptr);
+  dev_free(h, h->tiles_d, nullptr);
+  dev_free(h, h->slabs_d, nullptr);
+  dev_free(h, h->err_d, nullptr);
+  cudaDeviceSynchronize();
+  if (h->host_pinned) cudaFreeHost(h->host_pinned);
+  delete h;
+}
+
+int mf_compress(mf_bsr_t h, int layer, const void* q, const void* k, int dtype, int T, int H_s,
+                int H_ks, int d, int B, float p, int causal, void* stream) {
+  if (!h) return fail(MF_ERR_ARG, "handle is NULL");
+  if (layer < 0 || layer >= h->n_layers) return fail(MF_ERR_ARG, "layer %d out of range", layer);
+  if (!q || !k) return fail(MF_ERR_ARG, "q and k must be non-NULL");
+  if (T != h->T || H_s != h->H_s || B != h->B || causal != h->causal)
+    return fail(MF_ERR_ARG, "T/H_s/B/causal differ from the handle's");
+  if (H_ks < 1 || H_s % H_ks != 0) return fail(MF_ERR_ARG, "H_s %% H_ks != 0");
+  if (!(p > 0.f && p <= 1.f)) return fail(MF_ERR_ARG, "p must be in (0, 1]");
+  if (dtype != MF_DTYPE_BF16 && dtype != MF_DTYPE_F32) return fail(MF_ERR_ARG, "unknown dtype");
+  if (!check_shapes(dtype, d, B))
+    return fail(MF_ERR_UNSUPPORTED, "dtype %d with d = %d, B = %d is not built", dtype, d, B);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  LayerState& L = h->layers[layer];
+  if (L.meta || L.values || L.col_idx) release_layer(h, L, s);
+
+  const size_t HC = (size_t)h->H_s * h->C, HT = (size_t)h->H_s * h->T, HR = (size_t)h->H_s * h->R;
+  size_t off = 0;
+  const size_t o_mass = off; off += align_up(HC * 4);
+  const size_t o_max = off; off += align_up(HT * 4);
+  const size_t o_sum = off; off += align_up(HT * 4);
+  const size_t o_kc = off; off += align_up(HR * 4);
+  const size_t o_kept = off; off += align_up(HC * 4);
+  const size_t o_rp = off; off += align_up((HR + 1) * 4);
+  const size_t o_tile = off; off += align_up(HC * 4);
+  const size_t o_uc = off; off += align_up((size_t)h->R * 4);
+  const size_t o_ul = off; off += align_up((size_t)h->C * 4);
+  const size_t o_nnz = off; off += 256;
+  L.meta = dev_alloc(h, off, s);
+  if (!L.meta) return fail(MF_ERR_OOM, "allocation of %zu bytes failed", off);
+  L.meta_bytes = off;
+  char* mb = static_cast<char*>(L.meta);
+  L.mass = (float*)(mb + o_mass);
+  L.row_max = (float*)(mb + o_max);
+  L.row_sum = (float*)(mb + o_sum);
+  L.kcount = (int*)(mb + o_kc);
+  L.keptcols = (int*)(mb + o_kept);
+  L.row_ptr = (int*)(mb + o_rp);
+  L.tile_of = (int*)(mb + o_tile);
+  L.union_cnt = (int*)(mb + o_uc);
+  L.union_list = (int*)(mb + o_ul);
+  L.nnz_dev = (long long*)(mb + o_nnz);
+
+  CompressParams cp{};
+  cp.rbs = h->rbs_d;
+  cp.tiles = h->tiles_d;
+  cp.n_tiles = h->n_tiles;
+  cp.T = T;
+  cp.H_s = H_s;
+  cp.H_ks = H_ks;
+  cp.d = d;
+  cp.B = B;
+  cp.causal = causal;
+  cp.R = h->R;
+  cp.C = h->C;
+  cp.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d));
+  cp.p = p;
+  cp.mass = L.mass;
+  cp.row_max = L.row_max;
+  cp.row_sum = L.row_sum;
+  cp.kcount = L.kcount;
+  cp.keptcols = L.keptcols;
+  cp.row_ptr = L.row_ptr;
+  cp.tile_of = L.tile_of;
+  cp.union_cnt = L.union_cnt;
+  cp.union_list = L.union_list;
+  cp.nnz_out = L.nnz_dev;
+  cp.err = h->err_d;
+
+  CUtensorMap tq{}, tk{}, tk_pack{};
+  int rc;
+  if (dtype == MF_DTYPE_BF16) {
+    if ((reinterpret_cast<uintptr_t>(q) & 15) || (reinterpret_cast<uintptr_t>(k) & 15))
+      return fail(MF_ERR_ARG, "q and k must be 16-byte aligned");
+    if ((rc = make_map(&tq, q, (uint64_t)H_s * d, T, (uint64_t)H_s * d * 2, 64, 128)) != MF_OK) return rc;
+    if ((rc = make_map(&tk, k, (uint64_t)H_ks * d, T, (uint64_t)H_ks * d * 2, 64, 128)) != MF_OK) return rc;
+    if ((rc = make_map(&tk_pack, k, (uint64_t)H_ks * d, T, (uint64_t)H_ks * d * 2, 64, B)) != MF_OK) return rc;
+    MF_CUDA(launch_stats_bf16(cp, tq, tk, s), "statistics kernel");
+  } else {
+    MF_CUDA(launch_stats_f32(cp, (const float*)q, (const float*)k, s), "statistics kernel (fp32)");
+  }
+  MF_CUDA(launch_select(cp, s), "selection kernel");
+  MF_CUDA(launch_scan(cp, s), "row_ptr scan kernel");
+  MF_CUDA(cudaMemcpyAsync(&h->host_pinned[0], L.nnz_dev, sizeof(long long), cudaMemcpyDeviceToHost, s),
+          "nnz copy");
+  MF_CUDA(cudaMemcpyAsync(&h->host_pinned[1], h->err_d, sizeof(int), cudaMemcpyDeviceToHost, s),
+          "error word copy");
+  MF_CUDA(cudaStreamSynchronize(s), "compress sync");
+  const int dev_err = static_cast<int>(h->host_pinned[1] & 0xffffffff);
+  if (dev_err) {
+    cudaMemsetAsync(h->err_d, 0, sizeof(int), s);
+    release_layer(h, L, s);
+    return fail(MF_ERR_TIMEOUT, "a device-side wait timed out in the compressor");
+  }
+  const long long nnz = h->host_pinned[0];
+  L.nnz = nnz;
+  L.values_bytes = (size_t)nnz * B * B * 2;
+  L.colidx_bytes = (size_t)nnz * 4;
+  L.values = (uint16_t*)dev_alloc(h, L.values_bytes, s);
+  L.col_idx = (int*)dev_alloc(h, L.colidx_bytes, s);
+  if (!L.values || !L.col_idx) {
+    release_layer(h, L, s);
+    return fail(MF_ERR_OOM, "allocation of %zu bytes for the BSR values failed", L.values_bytes);
+  }
+  cp.col_idx = L.col_idx;
+  MF_CUDA(cudaMemsetAsync(L.tile_of, 0xFF, HC * 4, s), "tile index reset");
+  if (dtype == MF_DTYPE_BF16) {
+    CUtensorMap tvals{};
+    if (nnz > 0) {
+      if ((rc = make_map(&tvals, L.values, B, (uint64_t)nnz * B, (uint64_t)B * 2, 64,
+                         B == 64 ? 64 : 128)) != MF_OK)
+        return rc;
+      MF_CUDA(launch_pack_bf16(cp, tq, tk_pack, tvals, s), "pack kernel");
+    }
+  } else {
+    if (nnz > 0)
+      MF_CUDA(launch_pack_f32(cp, (const float*)q, (const float*)k, L.values, s), "pack kernel (fp32)");
+  }
+  MF_CUDA(launch_union(cp, s), "union kernel");
+  if (nnz > 0) {
+    if ((rc = make_map(&L.pmap, L.values, B, (uint64_t)nnz * B, (uint64_t)B * 2, 64, 64)) != MF_OK)
+      return rc;
+  }
+  L.valid = true;
+  L.dtype = dtype;
+  L.d = d;
+  L.p = p;
+  return MF_OK;
+}
+
+int mf_retrieve(mf_bsr_t h, const float* W, const void* v, void* o, int dtype, int H_r, int H_kv,
+                int d, const int32_t* layer_map_host, int n, void* stream) {
+  if (!h) return fail(MF_ERR_ARG, "handle is NULL");
+  if (!W || !v || !o || !layer_map_host) return fail(MF_ERR_ARG, "NULL pointer argument");
+  if (n < 1) return fail(MF_ERR_ARG, "n must be >= 1");
+  if (H_r < 1 || H_kv < 1 || H_r % H_kv != 0) return fail(MF_ERR_ARG, "H_r %% H_kv != 0");
+  if (dtype != MF_DTYPE_BF16 && dtype != MF_DTYPE_F32) return fail(MF_ERR_ARG, "unknown dtype");
+  if (!check_shapes(dtype, d, h->B))
+    return fail(MF_ERR_UNSUPPORTED, "dtype %d with d = %d, B = %d is not built", dtype, d, h->B);
+  const int hpg = H_r / H_kv;
+  if (dtype == MF_DTYPE_BF16 && hpg > 8)
+    return fail(MF_ERR_UNSUPPORTED, "H_r / H_kv = %d > 8", hpg);
+  if (dtype == MF_DTYPE_BF16 && ((reinterpret_cast<uintptr_t>(v) & 15) || (reinterpret_cast<uintptr_t>(o) & 15)))
+    return fail(MF_ERR_ARG, "v and o must be 16-byte aligned");
+  for (int x = 0; x < n; ++x) {
+    const int sl = layer_map_host[x];
+    if (sl < 0 || sl >= h->n_layers) return fail(MF_ERR_ARG, "layer_map[%d] = %d out of range", x, sl);
+    const LayerState& L = h->layers[sl];
+    if (!L.valid) return fail(MF_ERR_STATE, "sender layer %d has not been compressed", sl);
+    if (L.d != d) return fail(MF_ERR_ARG, "d = %d differs from the compressed layer's %d", d, L.d);
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t esz = (dtype == MF_DTYPE_BF16) ? 2 : 4;
+  const size_t v_layer = (size_t)h->T * H_kv * d * esz;
+  const size_t o_layer = (size_t)h->T * H_r * d * esz;
+  for (int x = 0; x < n; ++x) {
+    const LayerState& L = h->layers[layer_map_host[x]];
+    RetrieveParams rp{};
+    rp.rbs = h->rbs_d;
+    rp.slabs = h->slabs_d;
+    rp.n_slabs = h->n_slabs;
+    rp.T = h->T;
+    rp.H_s = h->H_s;
+    rp.H_r = H_r;
+    rp.H_kv = H_kv;
+    rp.d = d;
+    rp.B = h->B;
+    rp.R = h->R;
+    rp.C = h->C;
+    rp.tile_of = L.tile_of;
+    rp.union_cnt = L.union_cnt;
+    rp.union_list = L.union_list;
+    rp.W = W + (size_t)x * H_r * h->H_s;
+    rp.err = h->err_d;
+    const char* vx = static_cast<const char*>(v) + x * v_layer;
+    char* ox = static_cast<char*>(o) + x * o_layer;
+    if (dtype == MF_DTYPE_BF16) {
+      CUtensorMap tv{};
+      int rc = make_map(&tv, vx, (uint64_t)H_kv * d, h->T, (uint64_t)H_kv * d * 2, 64, 64);
+      if (rc != MF_OK) return rc;
+      CUtensorMap tp = L.pmap;
+      if (L.nnz == 0) tp = tv;  // never dereferenced: no block-row has a kept tile
+      MF_CUDA(launch_retrieve_bf16(rp, tp, tv, ox, s), "retrieval kernel");
+    } else {
+      MF_CUDA(launch_retrieve_f32(rp, L.values, (const float*)vx, (float*)ox, s),
+              "retrieval kernel (fp32)");
+    }
+  }
+  return MF_OK;
+}
+
+int mf_bsr_info(mf_bsr_t h, int layer, int64_t* nnz, int64_t* n_rows, int64_t* n_cand) {
+  if (!h) return fail(MF_ERR_ARG, "handle is NULL");
+  if (layer < 0 || layer >= h->n_layers) return fail(MF_ERR_ARG, "layer out of range");
+  const LayerState& L = h->layers[layer];
+  if (!L.valid) return fail(MF_ERR_STATE, "layer %d has not been compressed", layer);
+  if (nnz) *nnz = L.nnz;
+  if (n_rows) *n_rows = (int64_t)h->H_s * h->R;
+  if (n_cand) *n_cand = (int64_t)h->H_s * h->C;
+  return MF_OK;
+}
+
+int mf_bsr_export(mf_bsr_t h, int layer, const int32_t** row_ptr, const int32_t** col_idx,
+                  const uint16_t** values, const float** mass, const float** row_max,
+                  const float** row_sum) {
+  if (!h) return fail(MF_ERR_ARG, "handle is NULL");
+  if (layer < 0 || layer >= h->n_layers) return fail(MF_ERR_ARG, "layer out of range");
+  const LayerState& L = h->layers[layer];
+  if (!L.valid) return fail(MF_ERR_STATE, "layer %d has not been compressed", layer);
+  if (row_ptr) *row_ptr = L.row_ptr;
+  if (col_idx) *col_idx = L.col_idx;
+  if (values) *values = L.values;
+  if (mass) *mass = L.mass;
+  if (row_max) *row_max = L.row_max;
+  if (row_sum) *row_sum = L.row_sum;
+  return MF_OK;
+}
+
+int mf_bsr_copy(mf_bsr_t h, int layer, int32_t* row_ptr, int32_t* col_idx, uint16_t* values,
+                float* mass, float* row_max, float* row_sum, void* stream) {
+  if (!h) return fail(MF_ERR_ARG, "handle is NULL");
+  if (layer < 0 || layer >= h->n_layers) return fail(MF_ERR_ARG, "layer out of range");
+  const LayerState& L = h->layers[layer];
+  if (!L.valid) return fail(MF_ERR_STATE, "layer %d has not been compressed", layer);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t HR = (size_t)h->H_s * h->R, HC = (size_t)h->H_s * h->C, HT = (size_t)h->H_s * h->T;
+  auto cp = [&](void* dst, const void* src, size_t bytes) {
+    return (dst && bytes) ? cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, s) : cudaSuccess;
+  };
+  MF_CUDA(cp(row_ptr, L.row_ptr, (HR + 1) * 4), "row_ptr copy");
+  MF_CUDA(cp(col_idx, L.col_idx, L.colidx_bytes), "col_idx copy");
+  MF_CUDA(cp(values, L.values, L.values_bytes), "values copy");
+  MF_CUDA(cp(mass, L.mass, HC * 4), "mass copy");
+  MF_CUDA(cp(row_max, L.row_max, HT * 4), "row_max copy");
+  MF_CUDA(cp(row_sum, L.row_sum, HT * 4), "row_sum copy");
+  return MF_OK;
+}
+
+int mf_bsr_release_layer(mf_bsr_t h, int layer) {
+  if (!h) return fail(MF_ERR_ARG, "handle is NULL");
+  if (layer < 0 || layer >= h->n_layers) return fail(MF_ERR_ARG, "layer out of range");
+  release_layer(h, h->layers[layer], nullptr);
+  return MF_OK;
+}
+
+int mf_device_status(mf_bsr_t h, void* stream) {
+  if (!h) return fail(MF_ERR_ARG, "handle is NULL");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  MF_CUDA(cudaMemcpyAsync(&h->host_pinned[1], h->err_d, sizeof(int), cudaMemcpyDeviceToHost, s),
+          "error word copy");
+  MF_CUDA(cudaStreamSynchronize(s), "status sync");
+  const int e = static_cast<int>(h->host_pinned[1] & 0xffffffff);
+  if (e) {
+    cudaMemsetAsync(h->err_d, 0, sizeof(int), s);
+    cudaStreamSynchronize(s);
+    return fail(MF_ERR_TIMEOUT, "a device-side wait timed out");
+  }
+  return MF_OK;
+}
+
+int mf_selftest_wait(mf_bsr_t h, int limit_ms, void* stream) {
+  if (!h) return fail(MF_ERR_ARG, "handle is NULL");
+  if (limit_ms < 1 || limit_ms > 10000) return fail(MF_ERR_ARG, "limit_ms must be in [1, 10000]");
+  MF_CUDA(launch_selftest_wait(h->err_d, (unsigned long long)limit_ms * 1000000ull,
+                               static_cast<cudaStream_t>(stream)),
+          "self-test kernel");
+  return MF_OK;
+}
+
+}  // extern "C"

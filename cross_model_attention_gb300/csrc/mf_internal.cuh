@@ -1,0 +1,90 @@
+// mf_internal.cuh — shared host/device structures and kernel launchers of
+// libmapflow (not part of the public ABI).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace mf {
+
+// One global block-row (a B-row block of one packed sequence).
+struct RowBlock {
+  int seq_start;  // first token of the sequence in the packed batch
+  int L;          // sequence length
+  int bi;         // block-row index within the sequence
+  int cand_off;   // offset of this block-row's candidates in a head's mass row
+};
+
+// One 128-query-row tile of a sequence (the compressor's CTA unit).
+struct RowTile {
+  int seq_start;
+  int L;
+  int tl;   // tile index within the sequence (rows 128*tl .. 128*tl+127)
+  int rb0;  // global block-row of the tile's first block-row
+};
+
+// One 64-row slab of a block-row (the retrieval's CTA unit).
+struct RowSlab {
+  int rb;    // global block-row
+  int half;  // 0 for B = 64; 0/1 for B = 128
+};
+
+struct CompressParams {
+  const RowBlock* rbs;
+  const RowTile* tiles;
+  int n_tiles;
+  int T, H_s, H_ks, d, B, causal;
+  int R;            // block-rows
+  int C;            // candidates per head
+  float scale_log2; // log2(e) / sqrt(d)
+  float p;
+  // outputs / intermediates
+  float* mass;      // [H_s][C]
+  float* row_max;   // [H_s][T]  natural-log units
+  float* row_sum;   // [H_s][T]
+  int* kcount;      // [H_s*R]
+  int* keptcols;    // [H_s][C]  per row: kept block columns, ascending
+  int* row_ptr;     // [H_s*R + 1]
+  int* col_idx;     // [nnz]
+  int* tile_of;     // [C][H_s]  tile index of (block-row cand, head) or -1
+  int* union_cnt;   // [R]
+  int* union_list;  // [C]
+  long long* nnz_out;  // device scalar
+  int* err;
+};
+
+struct RetrieveParams {
+  const RowBlock* rbs;
+  const RowSlab* slabs;
+  int n_slabs;
+  int T, H_s, H_r, H_kv, d, B;
+  int R, C;
+  const int* tile_of;     // [C][H_s]
+  const int* union_cnt;   // [R]
+  const int* union_list;  // [C]
+  const float* W;         // [H_r][H_s] of this receiver layer
+  int* err;
+};
+
+// -------------------------------------------------------------- launchers --
+// All return cudaError_t of the launch (cudaSuccess when enqueued).
+cudaError_t launch_stats_bf16(const CompressParams& p, const CUtensorMap& tq,
+                              const CUtensorMap& tk, cudaStream_t s);
+cudaError_t launch_stats_f32(const CompressParams& p, const float* q, const float* k,
+                             cudaStream_t s);
+cudaError_t launch_select(const CompressParams& p, cudaStream_t s);
+cudaError_t launch_scan(const CompressParams& p, cudaStream_t s);
+cudaError_t launch_pack_bf16(const CompressParams& p, const CUtensorMap& tq,
+                             const CUtensorMap& tk, const CUtensorMap& tvals,
+                             cudaStream_t s);
+cudaError_t launch_pack_f32(const CompressParams& p, const float* q, const float* k,
+                            uint16_t* values, cudaStream_t s);
+cudaError_t launch_union(const CompressParams& p, cudaStream_t s);
+cudaError_t launch_retrieve_bf16(const RetrieveParams& p, const CUtensorMap& tp,
+                                 const CUtensorMap& tv, void* o, cudaStream_t s);
+cudaError_t launch_retrieve_f32(const RetrieveParams& p, const uint16_t* values, const float* v,
+                                float* o, cudaStream_t s);
+
+cudaError_t launch_selftest_wait(int* err, unsigned long long limit_ns, cudaStream_t s);
+
+}  // namespace mf

@@ -1,0 +1,313 @@
+// mf_pack_tc.cu — Attention State Compressor, step 3: pack the kept
+// probability tiles into Block Sparse Row form, bf16 inputs, sm_103a.
+//
+// "Accelerating Cross-Model LLM Inference via Attention Map Reuse", section
+// "Practical Implementation Details": the filtered map is stored in a compact
+// Block Sparse Row layout.  Row statistics m_i, l_i come from the statistics
+// pass; here only the kept tiles are recomputed (Q.K^T on tcgen05 into TMEM),
+// normalised, P_ij = 2^(s_ij*log2(e)/sqrt(d) - m_i*log2(e)) / l_i, rounded to
+// bf16 and written with TMA tensor stores from a 128-byte-swizzled staging
+// tile (so that every HBM write is a full, coalesced line).
+//
+// CTA = (128 query rows = one or two block-rows, one sender head); it walks the
+// ascending union of the kept block columns of its block-rows.  Warp roles as
+// in the statistics kernel: warp 0 TMA loads, warp 1 tcgen05 issue, warps 2-5
+// one thread per query row.  The CTA also writes col_idx and the per-(block,
+// head) tile index used by the retrieval.
+#include <cmath>
+
+#include "mf_internal.cuh"
+#include "mf_ptx.cuh"
+
+namespace mf {
+namespace {
+
+constexpr int kRows = 128;
+constexpr int kMaxU = 264;
+
+template <int D, int BLK>
+struct PackLayout {
+  static constexpr int kQChunk = kRows * 128;
+  static constexpr int kQBytes = kRows * D * 2;
+  static constexpr int kKChunk = BLK * 128;            // BLK key rows x 64 bf16
+  static constexpr int kKBytes = BLK * D * 2;
+  static constexpr int kStages = 3;
+  static constexpr int kStageBytes = (BLK == 64) ? 2 * 64 * 128 : 2 * 128 * 128;  // staging
+  static constexpr int kQ = 0;
+  static constexpr int kK = kQ + kQBytes;
+  static constexpr int kStg = kK + kStages * kKBytes;
+  static constexpr int kU = kStg + kStageBytes;        // int [3][kMaxU]
+  static constexpr int kBar = kU + 3 * kMaxU * 4;
+  static constexpr int kSlot = kBar + 16 * 8;
+  static constexpr int kMisc = kSlot + 8;
+  static constexpr int kBytes = kMisc + 16 + 1024;
+};
+
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int* err) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, err) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (ok) mbar_try(bar, parity);
+  __syncwarp();
+  return ok != 0;
+}
+
+template <int D, int BLK>
+__global__ void __launch_bounds__(192, 1)
+    pack_bf16_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                     const __grid_constant__ CUtensorMap tvals, const CompressParams p) {
+  using Lay = PackLayout<D, BLK>;
+  constexpr int NS = Lay::kStages;
+  constexpr int kN = BLK;  // MMA N = key block width
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const RowTile tile = p.tiles[blockIdx.x];
+  const int h = blockIdx.y;
+  const int hk = h / (p.H_s / p.H_ks);
+  int* u_bj = reinterpret_cast<int*>(smem + Lay::kU);
+  int* u_pos0 = u_bj + kMaxU;
+  int* u_pos1 = u_pos0 + kMaxU;
+  volatile int* misc = reinterpret_cast<volatile int*>(smem + Lay::kMisc);  // [0]=n_u [1]=abort
+
+  const uint32_t barQ = sb + Lay::kBar;
+  auto barFull = [&](int s) { return sb + Lay::kBar + 8u * (1 + s); };
+  auto barEmpty = [&](int s) { return sb + Lay::kBar + 8u * (1 + NS + s); };
+  auto barSFull = [&](int b) { return sb + Lay::kBar + 8u * (1 + 2 * NS + b); };
+  auto barSEmpty = [&](int b) { return sb + Lay::kBar + 8u * (3 + 2 * NS + b); };
+  const uint32_t barDone = sb + Lay::kBar + 8u * (5 + 2 * NS);
+
+  // block-rows covered by this tile
+  const int nsub = kRows / BLK;  // 2 for B=64, 1 for B=128
+  int rbv[2], kc[2], base[2];
+  const int* kl[2];
+  for (int t = 0; t < 2; ++t) {
+    const bool exists = t < nsub && (tile.tl * kRows + t * BLK) < tile.L;
+    rbv[t] = exists ? tile.rb0 + t : -1;
+    if (exists) {
+      const RowBlock rbk = p.rbs[rbv[t]];
+      const int row = h * p.R + rbv[t];
+      kc[t] = p.kcount[row];
+      base[t] = p.row_ptr[row];
+      kl[t] = p.keptcols + static_cast<size_t>(h) * p.C + rbk.cand_off;
+    } else {
+      kc[t] = 0;
+      base[t] = 0;
+      kl[t] = nullptr;
+    }
+  }
+
+  if (threadIdx.x == 0) {
+    mbar_init(barQ, 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(barFull(s), 1);
+      mbar_init(barEmpty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(barSFull(b), 1);
+      mbar_init(barSEmpty(b), 4);
+    }
+    mbar_init(barDone, 1);
+    fence_mbar_init();
+    // ascending union of the kept lists with each list's position
+    int i0 = 0, i1 = 0, n = 0;
+    while ((i0 < kc[0] || i1 < kc[1]) && n < kMaxU) {
+      const int a = i0 < kc[0] ? kl[0][i0] : 0x7fffffff;
+      const int b = i1 < kc[1] ? kl[1][i1] : 0x7fffffff;
+      const int bj = a < b ? a : b;
+      u_bj[n] = bj;
+      u_pos0[n] = (a == bj) ? i0++ : -1;
+      u_pos1[n] = (b == bj) ? i1++ : -1;
+      ++n;
+    }
+    misc[0] = n;
+    misc[1] = 0;
+  }
+  // col_idx and the retrieval's tile index of every kept (block, head)
+  if (threadIdx.x >= 64) {
+    for (int t = 0; t < 2; ++t) {
+      if (rbv[t] < 0) continue;
+      const RowBlock rbk = p.rbs[rbv[t]];
+      for (int i = threadIdx.x - 64; i < kc[t]; i += 128) {
+        const int bj = kl[t][i];
+        p.col_idx[base[t] + i] = bj;
+        p.tile_of[static_cast<size_t>(rbk.cand_off + bj) * p.H_s + h] = base[t] + i;
+      }
+    }
+  }
+  if (warp == 1) tmem_alloc(sb + Lay::kSlot, 2 * kN < 32 ? 32 : 2 * kN);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + Lay::kSlot);
+  const int n_u = misc[0];
+
+  if (warp == 0) {
+    if (lane == 0) {
+      prefetch_tmap(&tq);
+      prefetch_tmap(&tk);
+      prefetch_tmap(&tvals);
+      if (n_u > 0) {
+        mbar_arrive_tx(barQ, Lay::kQBytes);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_2d(sb + Lay::kQ + c * Lay::kQChunk, &tq, h * D + c * 64,
+                      tile.seq_start + tile.tl * kRows, barQ);
+      }
+      int issued = 0;
+      for (int u = 0; u < n_u; ++u) {
+        const int s = u % NS;
+        if (!mbar_wait(barEmpty(s), ((u / NS) & 1) ^ 1, p.err)) {
+          misc[1] = 1;
+          break;
+        }
+        mbar_arrive_tx(barFull(s), Lay::kKBytes);
+        const uint32_t dst = sb + Lay::kK + s * Lay::kKBytes;
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_2d(dst + c * Lay::kKChunk, &tk, hk * D + c * 64,
+                      tile.seq_start + u_bj[u] * BLK, barFull(s));
+        issued = u + 1;
+      }
+      for (int u = (issued > NS ? issued - NS : 0); u < issued; ++u)
+        mbar_wait(barFull(u % NS), (u / NS) & 1, nullptr);
+      if (n_u > 0) mbar_wait(barQ, 0, nullptr);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(kRows, kN, false, false);
+      bool ok = (n_u == 0) || mbar_wait(barQ, 0, p.err);
+      for (int u = 0; ok && u < n_u; ++u) {
+        const int s = u % NS, b = u & 1;
+        if (!mbar_wait(barFull(s), (u / NS) & 1, p.err) ||
+            !mbar_wait(barSEmpty(b), ((u >> 1) & 1) ^ 1, p.err)) {
+          misc[1] = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t qa = sb + Lay::kQ, ka = sb + Lay::kK + s * Lay::kKBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          tc_mma(tmem + b * kN, sdesc_sw128(qa + (kk >> 2) * Lay::kQChunk + (kk & 3) * 32, 16, 1024),
+                 sdesc_sw128(ka + (kk >> 2) * Lay::kKChunk + (kk & 3) * 32, 16, 1024), idesc,
+                 kk > 0 ? 1u : 0u);
+        }
+        tc_commit(barEmpty(s));
+        tc_commit(barSFull(b));
+      }
+      tc_commit(barDone);
+      mbar_wait(barDone, 0, nullptr);
+    }
+  } else {
+    // ------------------------------------------------ normalise + store
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;
+    const int row_local = tile.tl * kRows + row;
+    const bool row_ok = row_local < tile.L;
+    const int sub = row / BLK;  // which block-row of the tile
+    const int rloc = row - sub * BLK;
+    const uint32_t trow = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+    const float sc = p.scale_log2;
+    float m2 = 0.f, invl = 0.f;
+    if (row_ok) {
+      const size_t o = static_cast<size_t>(h) * p.T + tile.seq_start + row_local;
+      m2 = p.row_max[o] * 1.4426950408889634f;
+      invl = 1.f / p.row_sum[o];
+    }
+    // staging: BLK=64 -> two 8 KB tiles (one per block-row half);
+    //          BLK=128 -> one 32 KB tile as two 64-column 16 KB boxes
+    const uint32_t stg = sb + Lay::kStg;
+    uint8_t* stg_g = smem + Lay::kStg;
+    const int grp_threads = (BLK == 64) ? 64 : 128;
+    const int bar_id = (BLK == 64) ? 2 + sub : 2;
+    const bool leader = (BLK == 64) ? (rloc == 0) : (row == 0);
+    for (int u = 0; u < n_u; ++u) {
+      const int b = u & 1;
+      if (!warp_wait(barSFull(b), (u >> 1) & 1, p.err)) break;
+      tc_fence_after();
+      float s[BLK];
+      {
+        uint32_t* r = reinterpret_cast<uint32_t*>(s);
+#pragma unroll
+        for (int c = 0; c < BLK; c += 32) tmem_ld32(trow + b * kN + c, r + c);
+      }
+      tc_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(barSEmpty(b));
+      const int pos = (sub == 0) ? u_pos0[u] : u_pos1[u];
+      if (pos < 0) continue;  // this block-row does not keep the block (group-uniform)
+      const int bj = u_bj[u];
+      // wait until the previous store has finished reading the staging tile
+      if (leader) bulk_wait_read_all();
+      named_bar(bar_id, grp_threads);
+#pragma unroll
+      for (int c8 = 0; c8 < BLK / 8; ++c8) {
+        float v[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int c = c8 * 8 + e;
+          const int j = bj * BLK + c;
+          const bool vis = row_ok && (j < tile.L) && (!p.causal || j <= row_local);
+          v[e] = vis ? ex2(fmaf(s[c], sc, -m2)) * invl : 0.f;
+        }
+        uint4 w;
+        w.x = pack_bf16x2(v[0], v[1]);
+        w.y = pack_bf16x2(v[2], v[3]);
+        w.z = pack_bf16x2(v[4], v[5]);
+        w.w = pack_bf16x2(v[6], v[7]);
+        uint32_t off;
+        if (BLK == 64) off = sub * 8192 + sw128_off(rloc, c8);
+        else off = (c8 >> 3) * 16384 + sw128_off(row, c8 & 7);
+        *reinterpret_cast<uint4*>(stg_g + off) = w;
+      }
+      fence_async_smem();
+      named_bar(bar_id, grp_threads);
+      if (leader) {
+        const int tidx = ((sub == 0) ? base[0] : base[1]) + pos;
+        if (BLK == 64) {
+          tma_store_2d(&tvals, stg + sub * 8192, 0, tidx * 64);
+        } else {
+          tma_store_2d(&tvals, stg, 0, tidx * 128);
+          tma_store_2d(&tvals, stg + 16384, 64, tidx * 128);
+        }
+        bulk_commit();
+      }
+    }
+    if (leader) bulk_wait_all();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 2 * kN < 32 ? 32 : 2 * kN);
+  }
+}
+
+template <int D, int BLK>
+cudaError_t launch_pack_t(const CompressParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                          const CUtensorMap& tv, cudaStream_t s) {
+  auto kern = pack_bf16_kernel<D, BLK>;
+  const int smem = PackLayout<D, BLK>::kBytes;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(p.n_tiles, p.H_s);
+  kern<<<grid, 192, smem, s>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_pack_bf16(const CompressParams& p, const CUtensorMap& tq,
+                             const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t s) {
+  if (p.d == 128 && p.B == 64) return launch_pack_t<128, 64>(p, tq, tk, tv, s);
+  if (p.d == 128 && p.B == 128) return launch_pack_t<128, 128>(p, tq, tk, tv, s);
+  if (p.d == 64 && p.B == 64) return launch_pack_t<64, 64>(p, tq, tk, tv, s);
+  if (p.d == 64 && p.B == 128) return launch_pack_t<64, 128>(p, tq, tk, tv, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace mf

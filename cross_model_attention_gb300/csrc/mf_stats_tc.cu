@@ -1,0 +1,359 @@
+// mf_stats_tc.cu — Attention State Compressor, step 1 (block statistics) on
+// the sm_103a tensor cores, bf16 inputs.
+//
+// "Accelerating Cross-Model LLM Inference via Attention Map Reuse", section
+// "Practical Implementation Details": the compressor filters the sender's map
+// before caching it with block-level top-p; the news article
+// "北大MapFlow：注意力图跨模型复用，prefill延迟降15%–20%", paragraph "其一",
+// adds that it first computes block-level statistics and only then picks
+// blocks, never laying out the dense N x N map.  This kernel produces those
+// statistics in ONE pass over Q.K^T:
+//   row max m_i and row sum l_i of the causal softmax of s_ij = q_i.k_j/sqrt(d),
+//   and the probability mass of every candidate B x B block.
+//
+// CTA = (128 query rows of one sequence, one sender head).  Warp roles:
+//   warp 0  TMA producer: Q tile once, K tiles (128 keys) into a 3-4 stage ring
+//   warp 1  tcgen05 issuer: S = Q.K^T (M=128, N=128, K=d) into one of two TMEM
+//           buffers (fp32, 128 lanes x 128 columns each)
+//   warps 2-5  statistics, one thread per query row (its TMEM lane):
+//           block max, lazily re-referenced exp2, per-(row, key-block) partial
+//           sums written to TMEM columns 256..511 (so at most 256 key blocks per
+//           row), running row sum.  A row's reference value only moves when the
+//           block max exceeds it by more than 2^8; the stored partials of the
+//           warp are then rescaled in TMEM.
+//   end:    mass[bi][bj] = sum over the block-row's rows of partial/l_ref,
+//           reduced across lanes with a 31-shuffle transpose-reduction and
+//           across warps in a fixed order (deterministic).
+#include <cmath>
+
+#include "mf_internal.cuh"
+#include "mf_ptx.cuh"
+
+namespace mf {
+namespace {
+
+constexpr int kRows = 128;
+constexpr int kCols = 128;
+constexpr uint32_t kPartCol = 256;
+constexpr float kTau = 8.0f;
+constexpr float kLn2 = 0.69314718055994530942f;
+
+template <int D>
+struct StatsLayout {
+  static constexpr int kChunkBytes = kRows * 128;           // 128 rows x 64 bf16
+  static constexpr int kTileBytes = kRows * D * 2;
+  static constexpr int kStages = (D == 128) ? 3 : 4;
+  static constexpr int kQ = 0;
+  static constexpr int kK = kQ + kTileBytes;
+  static constexpr int kRed = kK + kStages * kTileBytes;    // float [4][256]
+  static constexpr int kBar = kRed + 4 * 256 * 4;           // 16 mbarriers
+  static constexpr int kSlot = kBar + 16 * 8;
+  static constexpr int kFlag = kSlot + 8;
+  static constexpr int kBytes = kFlag + 8 + 1024;           // + alignment slack
+};
+
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int* err) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, err) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (ok) mbar_try(bar, parity);  // every lane observes the completed phase
+  __syncwarp();
+  return ok != 0;
+}
+
+// Sum v[0..31] across the 32 lanes; on return lane l holds the total of
+// element l.  31 shuffles instead of 32*5.
+__device__ __forceinline__ float transpose_reduce32(float (&v)[32]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int w = 16; w >= 1; w >>= 1) {
+    const bool upper = (lane & w) != 0;
+#pragma unroll
+    for (int i = 0; i < w; ++i) {
+      const float send = upper ? v[i] : v[i + w];
+      const float keep = upper ? v[i + w] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+    }
+  }
+  return v[0];
+}
+
+__device__ __forceinline__ void rescale_parts(uint32_t taddr, int ncols, float alpha) {
+  int c = 0;
+  for (; c + 16 <= ncols; c += 16) {
+    uint32_t v[16];
+    tmem_ld16(taddr + c, v);
+    tc_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+        "%13,%14,%15,%16};" ::"r"(taddr + c),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+        "r"(v[15])
+        : "memory");
+  }
+  for (; c < ncols; ++c) {
+    uint32_t v;
+    tmem_ld1(taddr + c, v);
+    tc_wait_ld();
+    tmem_st1(taddr + c, __float_as_uint(__uint_as_float(v) * alpha));
+  }
+  tc_wait_st();
+}
+
+template <int D, int BLK>
+__global__ void __launch_bounds__(192, 1)
+    stats_bf16_kernel(const __grid_constant__ CUtensorMap tq,
+                      const __grid_constant__ CUtensorMap tk, const CompressParams p) {
+  using Lay = StatsLayout<D>;
+  constexpr int NS = Lay::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const RowTile tile = p.tiles[blockIdx.x];
+  const int h = blockIdx.y;
+  const int hk = h / (p.H_s / p.H_ks);
+  const int n_ct = p.causal ? tile.tl + 1 : (tile.L + kCols - 1) / kCols;
+
+  const uint32_t barQ = sb + Lay::kBar;
+  auto barFull = [&](int s) { return sb + Lay::kBar + 8u * (1 + s); };
+  auto barEmpty = [&](int s) { return sb + Lay::kBar + 8u * (1 + NS + s); };
+  auto barSFull = [&](int b) { return sb + Lay::kBar + 8u * (1 + 2 * NS + b); };
+  auto barSEmpty = [&](int b) { return sb + Lay::kBar + 8u * (3 + 2 * NS + b); };
+  const uint32_t barDone = sb + Lay::kBar + 8u * (5 + 2 * NS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::kFlag);
+
+  if (threadIdx.x == 0) {
+    mbar_init(barQ, 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(barFull(s), 1);
+      mbar_init(barEmpty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(barSFull(b), 1);
+      mbar_init(barSEmpty(b), 4);
+    }
+    mbar_init(barDone, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(sb + Lay::kSlot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + Lay::kSlot);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&tq);
+      prefetch_tmap(&tk);
+      const int qrow = tile.seq_start + tile.tl * kRows;
+      mbar_arrive_tx(barQ, Lay::kTileBytes);
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c)
+        tma_load_2d(sb + Lay::kQ + c * Lay::kChunkBytes, &tq, h * D + c * 64, qrow, barQ);
+      int issued = 0;
+      for (int n = 0; n < n_ct; ++n) {
+        const int s = n % NS;
+        if (!mbar_wait(barEmpty(s), ((n / NS) & 1) ^ 1, p.err)) {
+          *abort_flag = 1;
+          break;
+        }
+        mbar_arrive_tx(barFull(s), Lay::kTileBytes);
+        const uint32_t dst = sb + Lay::kK + s * Lay::kTileBytes;
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_2d(dst + c * Lay::kChunkBytes, &tk, hk * D + c * 64,
+                      tile.seq_start + n * kCols, barFull(s));
+        issued = n + 1;
+      }
+      // drain: copies still in flight complete before the CTA may exit
+      for (int n = (issued > NS ? issued - NS : 0); n < issued; ++n)
+        mbar_wait(barFull(n % NS), (n / NS) & 1, nullptr);
+      mbar_wait(barQ, 0, nullptr);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(kRows, kCols, false, false);
+      bool ok = mbar_wait(barQ, 0, p.err);
+      for (int n = 0; ok && n < n_ct; ++n) {
+        const int s = n % NS, b = n & 1;
+        if (!mbar_wait(barFull(s), (n / NS) & 1, p.err) ||
+            !mbar_wait(barSEmpty(b), ((n >> 1) & 1) ^ 1, p.err)) {
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t qa = sb + Lay::kQ, ka = sb + Lay::kK + s * Lay::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * Lay::kChunkBytes + (kk & 3) * 32;
+          tc_mma(tmem + b * kCols, sdesc_sw128(qa + off, 16, 1024),
+                 sdesc_sw128(ka + off, 16, 1024), idesc, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(barEmpty(s));
+        tc_commit(barSFull(b));
+      }
+      tc_commit(barDone);
+      mbar_wait(barDone, 0, nullptr);
+    }
+  } else {
+    // ---------------------------------------------------------- statistics
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;
+    const int row_local = tile.tl * kRows + row;
+    const bool row_ok = row_local < tile.L;
+    const uint32_t trow = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+    const float sc = p.scale_log2;
+    float mtrue = -INFINITY, ref = -INFINITY, lsum = 0.f;
+    int nblk = 0;
+    bool ok = true;
+    for (int n = 0; n < n_ct; ++n) {
+      const int b = n & 1;
+      if (!warp_wait(barSFull(b), (n >> 1) & 1, p.err)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float s[kCols];
+      {
+        uint32_t* r = reinterpret_cast<uint32_t*>(s);
+#pragma unroll
+        for (int c = 0; c < kCols; c += 32) tmem_ld32(trow + b * kCols + c, r + c);
+      }
+      tc_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(barSEmpty(b));
+      const bool last = (n == n_ct - 1);
+#pragma unroll
+      for (int hb = 0; hb < kCols / BLK; ++hb) {
+        float* x = s + hb * BLK;
+        const int col0 = n * kCols + hb * BLK;
+        float bm = -INFINITY;
+        if (last) {
+#pragma unroll
+          for (int c = 0; c < BLK; ++c) {
+            const int j = col0 + c;
+            const bool vis = (j < tile.L) && (!p.causal || j <= row_local);
+            x[c] = vis ? x[c] * sc : -INFINITY;
+            bm = fmaxf(bm, x[c]);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < BLK; ++c) {
+            x[c] *= sc;
+            bm = fmaxf(bm, x[c]);
+          }
+        }
+        if (!row_ok) bm = -INFINITY;
+        mtrue = fmaxf(mtrue, bm);
+        float alpha = 1.f;
+        if (bm > ref + kTau) {
+          alpha = (ref == -INFINITY) ? 0.f : ex2(ref - bm);
+          ref = bm;
+          lsum *= alpha;
+        }
+        if (__any_sync(0xffffffffu, alpha != 1.f) && nblk > 0) {
+          tc_wait_st();
+          rescale_parts(trow + kPartCol, nblk, alpha);
+        }
+        const float rs = (ref == -INFINITY) ? 0.f : ref;
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+        for (int c = 0; c < BLK; c += 4) {
+          a0 += ex2(x[c] - rs);
+          a1 += ex2(x[c + 1] - rs);
+          a2 += ex2(x[c + 2] - rs);
+          a3 += ex2(x[c + 3] - rs);
+        }
+        float bs = (a0 + a1) + (a2 + a3);
+        if (!row_ok) bs = 0.f;
+        lsum += bs;
+        tmem_st1(trow + kPartCol + nblk, __float_as_uint(bs));
+        ++nblk;
+      }
+    }
+    tc_wait_st();
+    // -------------------------------------------------------- epilogue
+    const bool good = ok && (*abort_flag == 0);
+    const float inv = (row_ok && lsum > 0.f) ? 1.f / lsum : 0.f;
+    if (good && row_ok) {
+      const size_t o = static_cast<size_t>(h) * p.T + tile.seq_start + row_local;
+      p.row_max[o] = mtrue * kLn2;
+      p.row_sum[o] = lsum * ex2(ref - mtrue);
+    }
+    float* red = reinterpret_cast<float*>(smem + Lay::kRed);
+    for (int c0 = 0; c0 < nblk; c0 += 32) {
+      uint32_t v[32];
+      tmem_ld32(trow + kPartCol + c0, v);
+      tc_wait_ld();
+      float f[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) f[i] = (c0 + i < nblk) ? __uint_as_float(v[i]) * inv : 0.f;
+      red[wq * 256 + c0 + lane] = transpose_reduce32(f);
+    }
+    tc_fence_before();
+    named_bar(1, 128);
+    if (good) {
+      const int t0 = threadIdx.x - 64;
+      if (BLK == 64) {
+        for (int t = t0; t < 2 * nblk; t += 128) {
+          const int half = t / nblk, c = t - half * nblk;
+          const int bi = tile.tl * 2 + half;
+          if (bi * 64 >= tile.L) continue;
+          const RowBlock rbk = p.rbs[tile.rb0 + half];
+          const int ncand = p.causal ? rbk.bi + 1 : (tile.L + 63) / 64;
+          if (c >= ncand) continue;
+          const float m = red[(2 * half) * 256 + c] + red[(2 * half + 1) * 256 + c];
+          p.mass[static_cast<size_t>(h) * p.C + rbk.cand_off + c] = m;
+        }
+      } else {
+        const RowBlock rbk = p.rbs[tile.rb0];
+        const int ncand = p.causal ? rbk.bi + 1 : (tile.L + BLK - 1) / BLK;
+        for (int c = t0; c < ncand; c += 128) {
+          const float m = (red[c] + red[256 + c]) + (red[512 + c] + red[768 + c]);
+          p.mass[static_cast<size_t>(h) * p.C + rbk.cand_off + c] = m;
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D, int BLK>
+cudaError_t launch_stats_t(const CompressParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                           cudaStream_t s) {
+  auto kern = stats_bf16_kernel<D, BLK>;
+  const int smem = StatsLayout<D>::kBytes;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(p.n_tiles, p.H_s);
+  kern<<<grid, 192, smem, s>>>(tq, tk, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_stats_bf16(const CompressParams& p, const CUtensorMap& tq,
+                              const CUtensorMap& tk, cudaStream_t s) {
+  if (p.d == 128 && p.B == 64) return launch_stats_t<128, 64>(p, tq, tk, s);
+  if (p.d == 128 && p.B == 128) return launch_stats_t<128, 128>(p, tq, tk, s);
+  if (p.d == 64 && p.B == 64) return launch_stats_t<64, 64>(p, tq, tk, s);
+  if (p.d == 64 && p.B == 128) return launch_stats_t<64, 128>(p, tq, tk, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace mf

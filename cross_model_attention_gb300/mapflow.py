@@ -1,0 +1,242 @@
+"""Thin ctypes binding of libmapflow (include/mapflow.h).
+
+Argument marshalling only: every step of the method runs in the CUDA
+library.  PyTorch supplies device memory (its caching allocator is handed to
+the library as the BSR allocator) and streams.  If the shared library is
+missing, importing this module raises: there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Dict, Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmapflow.so")
+
+MF_OK, MF_ERR_ARG, MF_ERR_UNSUPPORTED, MF_ERR_CUDA, MF_ERR_OOM, MF_ERR_TIMEOUT, MF_ERR_STATE = range(7)
+MF_DTYPE_F32, MF_DTYPE_BF16 = 0, 1
+
+EXPORTED = ("mf_version", "mf_last_error", "mf_supported", "mf_bsr_create", "mf_bsr_destroy",
+            "mf_compress", "mf_retrieve", "mf_bsr_info", "mf_bsr_export", "mf_bsr_copy",
+            "mf_bsr_release_layer", "mf_device_status", "mf_selftest_wait")
+
+
+class MapFlowError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"mapflow error {code}: {msg}")
+        self.code = code
+
+
+ALLOC_FN = ctypes.CFUNCTYPE(ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p)
+FREE_FN = ctypes.CFUNCTYPE(None, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p)
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libmapflow.so; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build it first "
+                          "(python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(path)
+    vp, i32, i64p = ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(ctypes.c_int64)
+    lib.mf_version.restype = i32
+    lib.mf_last_error.restype = ctypes.c_char_p
+    lib.mf_supported.argtypes = [i32, i32, i32]
+    lib.mf_bsr_create.argtypes = [ctypes.POINTER(vp), i32, i32, i32, i32, i32,
+                                  ctypes.POINTER(ctypes.c_int32), i32, ALLOC_FN, FREE_FN, vp]
+    lib.mf_bsr_destroy.argtypes = [vp]
+    lib.mf_bsr_destroy.restype = None
+    lib.mf_compress.argtypes = [vp, i32, vp, vp, i32, i32, i32, i32, i32, i32, ctypes.c_float,
+                                i32, vp]
+    lib.mf_retrieve.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32,
+                                ctypes.POINTER(ctypes.c_int32), i32, vp]
+    lib.mf_bsr_info.argtypes = [vp, i32, i64p, i64p, i64p]
+    lib.mf_bsr_export.argtypes = [vp, i32] + [ctypes.POINTER(vp)] * 6
+    lib.mf_bsr_copy.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp, vp]
+    lib.mf_bsr_release_layer.argtypes = [vp, i32]
+    lib.mf_device_status.argtypes = [vp, vp]
+    lib.mf_selftest_wait.argtypes = [vp, i32, vp]
+    for name in EXPORTED:
+        getattr(lib, name)
+    _lib = lib
+    return lib
+
+
+def _check(rc: int) -> None:
+    if rc != MF_OK:
+        raise MapFlowError(rc, load_library().mf_last_error().decode(errors="replace"))
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else int(t.data_ptr())
+
+
+def _stream(stream) -> Optional[int]:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return MF_DTYPE_BF16
+    if t.dtype == torch.float32:
+        return MF_DTYPE_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+# ------------------------------------------------------ torch allocator ----
+def _torch_allocator():
+    import torch
+
+    def _alloc(nbytes, ctx, stream):
+        try:
+            return torch.cuda.caching_allocator_alloc(int(nbytes), device=torch.cuda.current_device(),
+                                                      stream=stream or 0)
+        except Exception:  # noqa: BLE001 - signalled to the library as NULL
+            return None
+
+    def _free(ptr, ctx, stream):
+        if ptr:
+            torch.cuda.caching_allocator_delete(ptr)
+    return ALLOC_FN(_alloc), FREE_FN(_free)
+
+
+# --------------------------------------------- same names as the C ABI -----
+def mf_version() -> int:
+    return load_library().mf_version()
+
+
+def mf_supported(dtype: int, d: int, B: int) -> bool:
+    return bool(load_library().mf_supported(dtype, d, B))
+
+
+def mf_bsr_create(n_layers: int, T: int, H_s: int, B: int, causal: bool,
+                  cu_seqlens: Sequence[int], use_torch_allocator: bool = True):
+    """Returns (handle, keepalive); keepalive holds the allocator callbacks."""
+    lib = load_library()
+    cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
+    h = ctypes.c_void_p()
+    if use_torch_allocator:
+        a, f = _torch_allocator()
+    else:
+        a, f = ALLOC_FN(), FREE_FN()
+    rc = lib.mf_bsr_create(ctypes.byref(h), n_layers, T, H_s, B, int(causal),
+                           cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), len(cu) - 1,
+                           a, f, None)
+    _check(rc)
+    return h, (a, f)
+
+
+def mf_bsr_destroy(h) -> None:
+    load_library().mf_bsr_destroy(h)
+
+
+def mf_compress(h, layer: int, q, k, T: int, H_s: int, H_ks: int, d: int, B: int, p: float,
+                causal: bool, stream=None) -> None:
+    _check(load_library().mf_compress(h, layer, _ptr(q), _ptr(k), _dtype_code(q), T, H_s, H_ks,
+                                      d, B, float(p), int(causal), _stream(stream)))
+
+
+def mf_retrieve(h, W, v, o, H_r: int, H_kv: int, d: int, layer_map: Sequence[int],
+                stream=None) -> None:
+    lm = np.ascontiguousarray(np.asarray(layer_map, dtype=np.int32))
+    _check(load_library().mf_retrieve(h, _ptr(W), _ptr(v), _ptr(o), _dtype_code(v), H_r, H_kv, d,
+                                       lm.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), len(lm),
+                                       _stream(stream)))
+
+
+def mf_bsr_info(h, layer: int):
+    a, b, c = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+    _check(load_library().mf_bsr_info(h, layer, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)))
+    return a.value, b.value, c.value
+
+
+def mf_bsr_copy(h, layer: int, row_ptr=None, col_idx=None, values=None, mass=None,
+                row_max=None, row_sum=None, stream=None) -> None:
+    _check(load_library().mf_bsr_copy(h, layer, _ptr(row_ptr), _ptr(col_idx), _ptr(values),
+                                      _ptr(mass), _ptr(row_max), _ptr(row_sum), _stream(stream)))
+
+
+def mf_bsr_release_layer(h, layer: int) -> None:
+    _check(load_library().mf_bsr_release_layer(h, layer))
+
+
+def mf_device_status(h, stream=None) -> None:
+    _check(load_library().mf_device_status(h, _stream(stream)))
+
+
+def mf_selftest_wait(h, limit_ms: int, stream=None) -> None:
+    _check(load_library().mf_selftest_wait(h, int(limit_ms), _stream(stream)))
+
+
+# ------------------------------------------------------ convenience class --
+class BSR:
+    """Owner of one mf_bsr_t (compressed sender state of several layers)."""
+
+    def __init__(self, n_layers: int, T: int, H_s: int, B: int, cu_seqlens: Sequence[int],
+                 causal: bool = True, use_torch_allocator: bool = True):
+        self.n_layers, self.T, self.H_s, self.B, self.causal = n_layers, T, H_s, B, causal
+        self.cu_seqlens = [int(x) for x in cu_seqlens]
+        self.handle, self._keep = mf_bsr_create(n_layers, T, H_s, B, causal, self.cu_seqlens,
+                                                use_torch_allocator)
+        self.d: Optional[int] = None
+
+    def compress(self, layer: int, q, k, p: float, stream=None) -> None:
+        T, H_s, d = q.shape
+        self.d = d
+        mf_compress(self.handle, layer, q, k, T, H_s, k.shape[1], d, self.B, p, self.causal,
+                    stream)
+
+    def retrieve(self, W, v, o, layer_map: Sequence[int], stream=None) -> None:
+        n, T, H_kv, d = v.shape
+        H_r = o.shape[2]
+        mf_retrieve(self.handle, W, v, o, H_r, H_kv, d, layer_map, stream)
+
+    def info(self, layer: int):
+        return mf_bsr_info(self.handle, layer)
+
+    def export(self, layer: int, stream=None) -> Dict[str, "object"]:
+        """Copies of the layer's BSR arrays as torch tensors on the device."""
+        import torch
+        nnz, n_rows, n_cand = self.info(layer)
+        dev = torch.device("cuda", torch.cuda.current_device())
+        out = {
+            "row_ptr": torch.empty(n_rows + 1, dtype=torch.int32, device=dev),
+            "col_idx": torch.empty(max(nnz, 1), dtype=torch.int32, device=dev)[:nnz],
+            "values": torch.empty((max(nnz, 1), self.B, self.B), dtype=torch.bfloat16,
+                                  device=dev)[:nnz],
+            "mass": torch.empty(n_cand, dtype=torch.float32, device=dev),
+            "row_max": torch.empty((self.H_s, self.T), dtype=torch.float32, device=dev),
+            "row_sum": torch.empty((self.H_s, self.T), dtype=torch.float32, device=dev),
+        }
+        mf_bsr_copy(self.handle, layer, out["row_ptr"], out["col_idx"] if nnz else None,
+                    out["values"] if nnz else None, out["mass"], out["row_max"],
+                    out["row_sum"], stream)
+        return out
+
+    def release_layer(self, layer: int) -> None:
+        mf_bsr_release_layer(self.handle, layer)
+
+    def device_status(self, stream=None) -> None:
+        mf_device_status(self.handle, stream)
+
+    def close(self) -> None:
+        if self.handle is not None:
+            mf_bsr_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:  # noqa: BLE001
+            pass

@@ -1,0 +1,229 @@
+/*
+ * mapflow.h — C ABI of the GB300 (sm_103a) hot path of cross-model
+ * attention-map reuse.
+ *
+ * The method is described on two pages:
+ *   [Summary] "Accelerating Cross-Model LLM Inference via Attention Map Reuse"
+ *             (paper summary page), sections "MapFlow System Design",
+ *             "Practical Implementation Details" and bold headers 2-4;
+ *   [Article] "北大MapFlow：注意力图跨模型复用，prefill延迟降15%–20%" (news
+ *             article), the paragraphs "其一" (compressor: block statistics,
+ *             then block selection, no dense map) and "其三" (retrieval: heads
+ *             combined on chip, multiplied by the receiver's V, accumulated).
+ *
+ * Two calls carry the method:
+ *   mf_compress  — the Attention State Compressor: causal-softmax row
+ *                  statistics of a sender layer's Q.K^T/sqrt(d), B x B block
+ *                  masses, block-level top-p per (head, block-row), and the
+ *                  kept probability tiles packed as Block Sparse Row (BSR).
+ *   mf_retrieve  — the fused Attention Retrieval: for receiver layer j, reads
+ *                  the BSR of sender layer m(j), combines the sender heads as
+ *                  A_hat_i = sum_h W_j[i,h] * A_h on chip (missing blocks are
+ *                  zero, no renormalisation) and multiplies by the receiver's
+ *                  V of head i's KV group, accumulating O_i; no dense A_hat is
+ *                  ever written to memory.
+ *
+ * Conventions (all calls):
+ *   - Every pointer argument is a DEVICE pointer unless its name ends in
+ *     "_host".  The caller owns every buffer it passes; the handle owns the
+ *     BSR buffers it allocates (through the caller's allocator when one is
+ *     given, else cudaMallocAsync on the call's stream).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default).
+ *     Work is enqueued on it; calls return before the GPU finishes, except
+ *     where a call states that it synchronises.
+ *   - Every call returns an mf_status (MF_OK = 0).  Nothing throws across the
+ *     ABI.  On failure mf_last_error() returns a message (thread-local).
+ *   - Sequences are packed: token t of sequence s lives at row
+ *     cu_seqlens[s] + t of every [T, H, d] tensor.  Block grids start at each
+ *     sequence's first token; tiles never straddle sequences.
+ *   - Layouts are dense row-major: Q [T][H_s][d], K [T][H_ks][d],
+ *     V [T][H_kv][d], O [T][H_r][d], W [H_r][H_s].
+ *   - GQA grouping is contiguous: query head h uses KV head h / (H_q/H_kv).
+ *   - There is no CPU fallback: without a usable sm_103a GPU every compute
+ *     call fails with MF_ERR_CUDA.
+ */
+#ifndef MAPFLOW_H_
+#define MAPFLOW_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MF_API __attribute__((visibility("default")))
+#else
+#define MF_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define MF_OK              0
+#define MF_ERR_ARG         1  /* invalid argument (NULL, negative, inconsistent) */
+#define MF_ERR_UNSUPPORTED 2  /* valid but outside the compiled shapes        */
+#define MF_ERR_CUDA        3  /* CUDA runtime / launch error                  */
+#define MF_ERR_OOM         4  /* allocator returned NULL                      */
+#define MF_ERR_TIMEOUT     5  /* a device-side wait hit its limit             */
+#define MF_ERR_STATE       6  /* call order (e.g. retrieve before compress)   */
+
+/* ---- element types ------------------------------------------------------ */
+#define MF_DTYPE_F32  0   /* IEEE fp32                                      */
+#define MF_DTYPE_BF16 1   /* bfloat16 (stored as uint16)                    */
+
+typedef struct mf_bsr_s* mf_bsr_t;   /* opaque; owns BSR state of n layers */
+
+/* Optional caller allocator (e.g. a framework's caching allocator).  Must
+ * return a device pointer aligned to >= 256 bytes usable on `stream`, or
+ * NULL on failure.  `free_fn` releases a pointer returned by `alloc_fn`. */
+typedef void* (*mf_alloc_fn)(size_t bytes, void* ctx, void* stream);
+typedef void  (*mf_free_fn)(void* ptr, void* ctx, void* stream);
+
+/* Library version: major*10000 + minor*100 + patch. */
+MF_API int mf_version(void);
+
+/* Message of the last failed call on this thread ("" if none). */
+MF_API const char* mf_last_error(void);
+
+/* Supported shapes of this build (for callers that want to check first). */
+MF_API int mf_supported(int dtype, int d, int B);
+
+/*
+ * mf_bsr_create — create a handle that will hold the compressed attention
+ * state of `n_layers` sender layers over one packed batch.
+ *
+ *   n_layers          number of sender layers the handle can hold (>= 1)
+ *   T                 total packed tokens (= cu_seqlens_host[n_seqs])
+ *   H_s               sender query heads
+ *   B                 block size (64 or 128)
+ *   causal            1 = causal attention (candidates bj <= bi), 0 = full
+ *   cu_seqlens_host   HOST int32 [n_seqs+1], cu[0] = 0, non-decreasing,
+ *                     cu[n_seqs] = T; every sequence length <= 256*B
+ *   n_seqs            number of packed sequences (>= 1)
+ *   alloc_fn/free_fn  optional allocator pair (both NULL or both set)
+ *   alloc_ctx         passed back to the allocator
+ *
+ * Errors: MF_ERR_ARG on inconsistent arguments, MF_ERR_UNSUPPORTED on B or
+ * sequence lengths outside the build, MF_ERR_CUDA / MF_ERR_OOM when the small
+ * per-handle tables cannot be placed on the device.  Synchronous.
+ */
+MF_API int mf_bsr_create(mf_bsr_t* out, int n_layers, int T, int H_s, int B, int causal,
+                  const int32_t* cu_seqlens_host, int n_seqs,
+                  mf_alloc_fn alloc_fn, mf_free_fn free_fn, void* alloc_ctx);
+
+/* Release every buffer of the handle (waits for the device first). */
+MF_API void mf_bsr_destroy(mf_bsr_t h);
+
+/*
+ * mf_compress — Attention State Compressor for one sender layer
+ * ([Summary] "Practical Implementation Details"; [Article] "其一").
+ *
+ *   layer    0-based slot in the handle (< n_layers); an existing state in
+ *            that slot is released first
+ *   q        [T][H_s][d]  sender queries of the layer (dtype)
+ *   k        [T][H_ks][d] sender keys of the layer (dtype)
+ *   dtype    MF_DTYPE_BF16 (tensor-core path) or MF_DTYPE_F32
+ *   T,H_s,B,causal  must equal the handle's
+ *   H_ks     sender KV heads, H_s % H_ks == 0
+ *   d        head dimension, 64 or 128
+ *   p        top-p threshold, 0 < p <= 1
+ *
+ * Computes, per head h and row i, m_i = max_j s_ij and
+ * l_i = sum_j exp(s_ij - m_i) with s_ij = q_i.k_j/sqrt(d) over the keys the
+ * row may see; the probability mass of every candidate B x B block; the
+ * block-level top-p of every (head, block-row): sort by mass descending,
+ * ties to the lower block column, keep the shortest prefix whose cumulative
+ * mass reaches p of the row's total, evaluated exactly in fixed point
+ * (q_b = rint(mass_b * 2^32), P_q = rint(p * 2^20), keep the smallest k with
+ * 2^20 * sum_{t<k} q_(t) >= P_q * sum_b q_b); and the BSR of the kept tiles:
+ *   row_ptr int32 [H_s*R + 1]   rows ordered head-major, then global
+ *                               block-row (R = sum_s ceil(L_s/B))
+ *   col_idx int32 [nnz]         block column relative to the sequence's first
+ *                               block, ascending within a row
+ *   values  bf16  [nnz][B][B]   P_ij = exp(s_ij - m_i)/l_i, zero above the
+ *                               diagonal and outside the sequence
+ * It synchronises `stream` once (to size the values buffer from nnz).
+ * Errors: MF_ERR_ARG, MF_ERR_UNSUPPORTED, MF_ERR_OOM, MF_ERR_CUDA,
+ * MF_ERR_TIMEOUT (a device wait gave up; the layer is left empty).
+ */
+MF_API int mf_compress(mf_bsr_t h, int layer, const void* q, const void* k, int dtype,
+                int T, int H_s, int H_ks, int d, int B, float p, int causal,
+                void* stream);
+
+/*
+ * mf_retrieve — fused Attention Retrieval for n receiver layers
+ * ([Summary] "Practical Implementation Details" and bold header 4;
+ * [Article] "其三"; head mapping per [Summary] "MapFlow System Design" 3).
+ *
+ *   W               fp32 [n][H_r][H_s]  head-mapping weights of each layer
+ *   v               [n][T][H_kv][d]     receiver values (dtype)
+ *   o               [n][T][H_r][d]      output (dtype), fully overwritten
+ *   dtype           MF_DTYPE_BF16 or MF_DTYPE_F32 (must match the layer's
+ *                   compress dtype family: bf16 retrieval needs d in {64,128})
+ *   H_r, H_kv       receiver query / KV heads, H_r % H_kv == 0,
+ *                   H_r/H_kv <= 8 (d = 128) or <= 16 (d = 64)
+ *   d               head dimension (= the compressed layers' d)
+ *   layer_map_host  HOST int32 [n]: handle slot (sender layer) used by call
+ *                   layer x; each slot must hold a compressed state
+ *   n               number of receiver layers in this call (>= 1)
+ *
+ * O_i[t] = sum over the kept blocks (h, bi, bj) of block-row bi of t:
+ *          W[i,h] * P_h[t, bj cols] @ V_g(i)[bj rows], fp32 accumulation.
+ * Rows of blocks with no kept tile get O = 0.  Asynchronous.
+ * Errors: MF_ERR_ARG, MF_ERR_UNSUPPORTED, MF_ERR_STATE, MF_ERR_CUDA.
+ */
+MF_API int mf_retrieve(mf_bsr_t h, const float* W, const void* v, void* o, int dtype,
+                int H_r, int H_kv, int d, const int32_t* layer_map_host, int n,
+                void* stream);
+
+/*
+ * mf_bsr_info — sizes of a compressed layer: nnz (kept tiles), rows
+ * (H_s*R), candidates (H_s * sum of candidate blocks per block-row).
+ */
+MF_API int mf_bsr_info(mf_bsr_t h, int layer, int64_t* nnz, int64_t* n_rows, int64_t* n_cand);
+
+/*
+ * mf_bsr_export — device pointers (owned by the handle, valid until the
+ * layer is released or recompressed) to a compressed layer:
+ *   row_ptr  int32 [H_s*R+1], col_idx int32 [nnz], values bf16 [nnz][B][B],
+ *   mass     fp32 [H_s][C] candidate masses (per head: block-rows in global
+ *            order, each with its candidates bj = 0.. in order),
+ *   row_max  fp32 [H_s][T] (m_i), row_sum fp32 [H_s][T] (l_i).
+ * Any output pointer may be NULL.
+ */
+MF_API int mf_bsr_export(mf_bsr_t h, int layer, const int32_t** row_ptr, const int32_t** col_idx,
+                  const uint16_t** values, const float** mass, const float** row_max,
+                  const float** row_sum);
+
+/*
+ * mf_bsr_copy — copy a compressed layer into caller-owned DEVICE buffers
+ * (sizes as for mf_bsr_export; any destination may be NULL).  Asynchronous on
+ * `stream`.
+ */
+MF_API int mf_bsr_copy(mf_bsr_t h, int layer, int32_t* row_ptr, int32_t* col_idx, uint16_t* values,
+                float* mass, float* row_max, float* row_sum, void* stream);
+
+/* mf_bsr_release_layer — free one layer's state (per-layer streaming). */
+MF_API int mf_bsr_release_layer(mf_bsr_t h, int layer);
+
+/*
+ * mf_device_status — synchronise `stream` and read the handle's device
+ * error word (set by bounded device-side waits).  Returns MF_OK,
+ * MF_ERR_TIMEOUT (and clears the word), or MF_ERR_CUDA.
+ */
+MF_API int mf_device_status(mf_bsr_t h, void* stream);
+
+/*
+ * mf_selftest_wait — failure-detection self-test (no counterpart on the
+ * pages).  Launches one thread that waits on a device barrier nothing will
+ * complete, bounded by `limit_ms` milliseconds (1..10000); the wait gives up,
+ * records a timeout in the handle's device error word and returns, leaving
+ * the context usable.  A following mf_device_status returns MF_ERR_TIMEOUT.
+ */
+MF_API int mf_selftest_wait(mf_bsr_t h, int limit_ms, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif  /* MAPFLOW_H_ */

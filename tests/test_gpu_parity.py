@@ -1,0 +1,216 @@
+"""GPU parity: the CUDA path (through the C-ABI) against the fp64 oracle.
+
+Small cases span several tiles, ragged tails, packed sequences, GQA, odd
+heads-per-group, both block sizes and head dims, non-causal attention, p = 1
+and a p so small that no block is kept.  Full-size cases run each workload at
+its real sequence length and head counts (one sender layer) and compare
+sampled block-rows with the oracle; the selection is always checked on every
+row.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from cross_model_attention_gb300 import mapflow, synth, workloads
+from oracle import mapflow_oracle as orc
+from tests import gpu_cases as gc
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    gc.dev()
+
+
+def small_case(seqlens, Hs, Hks, d, B, p, Hr, Hkv, dtype="bf16", causal=True, seed=0,
+               structured=True, n_rlayers=1):
+    T = int(sum(seqlens))
+    cu = np.concatenate([[0], np.cumsum(seqlens)]).astype(np.int32)
+    if structured:
+        w = workloads.scaled(workloads.get(1), seqlens, sender_heads=Hs, sender_kv_heads=Hks,
+                             d=d, B=B, dtype=dtype, causal=causal, seed=seed)
+        x = synth.sender_qk(w, 1)
+    else:
+        x = synth.random_qk(T, Hs, Hks, d, seed, dtype=dtype)
+    vs = [synth.random_v(T, Hkv, d, seed + 10 + j, dtype=dtype) for j in range(n_rlayers)]
+    W = np.stack([synth.random_w(Hr, Hs, seed + 20 + j) for j in range(n_rlayers)])
+    bsr = mapflow.BSR(1, T, Hs, B, cu, causal=causal)
+    gc.run_compress(bsr, 0, x, dtype, p)
+    ex = gc.export_np(bsr, 0)
+    grid = orc.BlockGrid(cu, B, causal)
+    gc.check_structure(ex, grid, Hs, p)
+    pairs = [(h, rb) for h in range(Hs) for rb in range(grid.R)]
+    gc.check_block_rows(ex, x["q64"], x["k64"], grid, Hs, pairs)
+    O = gc.run_retrieve(bsr, W, np.stack([v["v"] for v in vs]), Hr, dtype, [0] * n_rlayers)
+    for j in range(n_rlayers):
+        gc.check_output(O[j], x["q64"], x["k64"], grid, ex, Hs, W[j], vs[j]["v64"], Hkv,
+                        range(grid.R))
+    bsr.close()
+    return ex
+
+
+@pytest.mark.parametrize("seqlens,Hs,Hks,d,B,Hr,Hkv", [
+    ((512,), 4, 4, 128, 64, 8, 2),            # several tiles, hpg 4
+    ((200, 137, 64, 1, 130), 4, 2, 128, 64, 6, 2),  # varlen, ragged, GQA, hpg 3
+    ((300, 129), 3, 3, 128, 128, 8, 2),       # B = 128, ragged
+    ((333,), 2, 1, 64, 64, 4, 4),             # d = 64, hpg 1
+    ((257, 64), 2, 2, 64, 128, 16, 2),        # d = 64, B = 128, hpg 8
+])
+def test_small_bf16(seqlens, Hs, Hks, d, B, Hr, Hkv):
+    small_case(seqlens, Hs, Hks, d, B, 0.95, Hr, Hkv)
+
+
+def test_noncausal():
+    small_case((190, 70), 2, 2, 128, 64, 4, 2, causal=False, structured=False)
+
+
+def test_p1_keeps_every_block_with_mass():
+    ex = small_case((384,), 2, 2, 128, 64, 4, 2, p=1.0)
+    # every causal candidate with non-zero fixed-point mass is kept
+    assert ex["row_ptr"][-1] > 0
+
+
+def test_nothing_kept_gives_zero_output():
+    # p * 2^20 rounds to 0: the threshold is 0, no block is needed
+    seqlens = (256,)
+    T = 256
+    x = synth.random_qk(T, 2, 2, 128, 3)
+    v = synth.random_v(T, 2, 128, 4)
+    W = synth.random_w(4, 2, 5)[None]
+    bsr = mapflow.BSR(1, T, 2, 64, [0, T])
+    gc.run_compress(bsr, 0, x, "bf16", 2e-7)
+    ex = gc.export_np(bsr, 0)
+    assert ex["row_ptr"][-1] == 0
+    O = gc.run_retrieve(bsr, W, v["v"][None], 4, "bf16", [0])
+    assert np.all(O == 0.0)
+    bsr.close()
+
+
+def test_unstructured_random_logits():
+    small_case((448,), 3, 3, 128, 64, 6, 3, p=0.9, structured=False, seed=7)
+
+
+def test_fp32_workload0():
+    """The fp32 workload exactly: N=512, H_s=4, d=64, B=64, p=0.95, W = I + N(0,1/4)."""
+    w = workloads.get(0)
+    x = synth.sender_qk(w, 1)
+    rcv = w.receivers[0]
+    v = synth.receiver_v(w, rcv, 1)
+    W = synth.head_map_weights(w, rcv, 1)
+    bsr = mapflow.BSR(1, w.T, w.sender_heads, w.B, w.cu_seqlens)
+    gc.run_compress(bsr, 0, x, "f32", w.p[0])
+    ex = gc.export_np(bsr, 0)
+    grid = orc.BlockGrid(w.cu_seqlens, w.B, True)
+    gc.check_structure(ex, grid, w.sender_heads, w.p[0])
+    gc.check_block_rows(ex, x["q64"], x["k64"], grid, w.sender_heads,
+                        [(h, rb) for h in range(4) for rb in range(grid.R)])
+    O = gc.run_retrieve(bsr, W[None], v["v"][None], rcv.heads, "f32", [0])
+    gc.check_output(O[0], x["q64"], x["k64"], grid, ex, 4, W, v["v64"], rcv.kv_heads,
+                    range(grid.R))
+    bsr.close()
+
+
+def test_multi_layer_map_and_determinism():
+    seqlens = (320, 200)
+    T = sum(seqlens)
+    cu = np.concatenate([[0], np.cumsum(seqlens)]).astype(np.int32)
+    w = workloads.scaled(workloads.get(1), seqlens, sender_heads=4, sender_kv_heads=4)
+    xs = [synth.sender_qk(w, l) for l in (1, 2)]
+    bsr = mapflow.BSR(2, T, 4, 64, cu)
+    for l in range(2):
+        gc.run_compress(bsr, l, xs[l], "bf16", 0.9)
+    ex0 = gc.export_np(bsr, 0)
+    # recompress layer 0: bit-identical BSR
+    gc.run_compress(bsr, 0, xs[0], "bf16", 0.9)
+    ex0b = gc.export_np(bsr, 0)
+    for key in ("row_ptr", "col_idx", "mass", "row_max", "row_sum"):
+        assert np.array_equal(ex0[key], ex0b[key]), key
+    assert torch.equal(ex0["values_dev"].view(torch.int16), ex0b["values_dev"].view(torch.int16))
+    ex1 = gc.export_np(bsr, 1)
+    vs = [synth.random_v(T, 2, 128, 40 + j) for j in range(3)]
+    W = np.stack([synth.random_w(8, 4, 50 + j) for j in range(3)])
+    lm = [1, 0, 1]
+    O = gc.run_retrieve(bsr, W, np.stack([v["v"] for v in vs]), 8, "bf16", lm)
+    grid = orc.BlockGrid(cu, 64, True)
+    for j, l in enumerate(lm):
+        gc.check_output(O[j], xs[l]["q64"], xs[l]["k64"], grid, (ex0, ex1)[l], 4, W[j],
+                        vs[j]["v64"], 2, range(grid.R))
+    bsr.close()
+
+
+def test_device_wait_timeout_is_reported():
+    """A bounded device wait that nothing completes returns MF_ERR_TIMEOUT
+    through the error word; the context stays usable."""
+    bsr = mapflow.BSR(1, 64, 1, 64, [0, 64])
+    mapflow.mf_selftest_wait(bsr.handle, 50)
+    with pytest.raises(mapflow.MapFlowError) as ei:
+        bsr.device_status()
+    assert ei.value.code == mapflow.MF_ERR_TIMEOUT
+    bsr.device_status()  # cleared
+    small_case((128,), 1, 1, 64, 64, 1, 1)  # the context still works
+    bsr.close()
+
+
+def test_retrieve_before_compress_is_rejected():
+    bsr = mapflow.BSR(1, 64, 1, 64, [0, 64])
+    W = torch.zeros((1, 1, 1), device=gc.dev())
+    v = torch.zeros((1, 64, 1, 64), dtype=torch.bfloat16, device=gc.dev())
+    o = torch.zeros((1, 64, 1, 64), dtype=torch.bfloat16, device=gc.dev())
+    with pytest.raises(mapflow.MapFlowError) as ei:
+        bsr.retrieve(W, v, o, [0])
+    assert ei.value.code == mapflow.MF_ERR_STATE
+    bsr.close()
+
+
+# ---------------------------------------------------------------- full size --
+
+def full_size(idx, p=None, sender_layer=None, n_rows=4, receivers=None):
+    w = workloads.get(idx)
+    p = w.p[0] if p is None else p
+    rcvs = w.receivers if receivers is None else receivers
+    layer = sender_layer or rcvs[0].layer_map(w.sender_layers)[0][1]
+    x = synth.sender_qk(w, layer)
+    bsr = mapflow.BSR(1, w.T, w.sender_heads, w.B, w.cu_seqlens)
+    gc.run_compress(bsr, 0, x, w.dtype, p)
+    ex = gc.export_np(bsr, 0)
+    grid = orc.BlockGrid(w.cu_seqlens, w.B, True)
+    gc.check_structure(ex, grid, w.sender_heads, p)
+    rbs = gc.sample_block_rows(grid, n_rows, 100 + idx)
+    rng = np.random.default_rng(idx)
+    pairs = [(int(rng.integers(w.sender_heads)), rb) for rb in rbs]
+    gc.check_block_rows(ex, x["q64"], x["k64"], grid, w.sender_heads, pairs)
+    res = {"kept_frac": ex["row_ptr"][-1] / (w.sender_heads * grid.C)}
+    for rcv in rcvs:
+        j = next(jj for jj, m in rcv.layer_map(w.sender_layers) if m == layer) \
+            if any(m == layer for _, m in rcv.layer_map(w.sender_layers)) else rcv.recompute + 1
+        v = synth.receiver_v(w, rcv, j)
+        W = synth.head_map_weights(w, rcv, j)
+        O = gc.run_retrieve(bsr, W[None], v["v"][None], rcv.heads, w.dtype, [0])
+        res[rcv.name] = gc.check_output(O[0], x["q64"], x["k64"], grid, ex, w.sender_heads, W,
+                                        v["v64"], rcv.kv_heads, rbs[:n_rows])
+        del O
+    bsr.close()
+    torch.cuda.empty_cache()
+    return res
+
+
+def test_full_workload1():
+    full_size(1)
+
+
+def test_full_workload2():
+    full_size(2)
+
+
+@pytest.mark.parametrize("p", [0.80, 0.99])
+def test_full_workload3(p):
+    full_size(3, p=p, n_rows=2)
+
+
+def test_full_workload4_two_receivers():
+    full_size(4)
