@@ -102,7 +102,16 @@ struct LayerState {
   CUtensorMap pmap;  // values as [nnz*B rows][B cols], 64x64 boxes (retrieval)
 };
 
+struct ProfRec {
+  int kind;
+  cudaEvent_t a, b;
+};
+
 struct mf_bsr_s {
+  bool profiling = false;
+  long long launches[MF_K_COUNT] = {0};
+  std::vector<ProfRec> prof;
+  std::vector<cudaEvent_t> event_pool;
   int n_layers = 0, T = 0, H_s = 0, B = 0, causal = 1, n_seqs = 0;
   int R = 0, C = 0, n_tiles = 0, n_slabs = 0;
   std::vector<int> cu;
@@ -147,6 +156,34 @@ void release_layer(mf_bsr_t h, LayerState& L, cudaStream_t s) {
 }
 
 size_t align_up(size_t x) { return (x + 255) & ~size_t(255); }
+
+cudaEvent_t take_event(mf_bsr_t h) {
+  if (!h->event_pool.empty()) {
+    cudaEvent_t e = h->event_pool.back();
+    h->event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return e;
+}
+
+// Runs one kernel launch, counting it and (when profiling) bracketing it with
+// events on its stream.
+template <typename F>
+cudaError_t timed(mf_bsr_t h, int kind, cudaStream_t s, F&& launch) {
+  h->launches[kind] += 1;
+  if (!h->profiling) return launch();
+  cudaEvent_t a = take_event(h), b = take_event(h);
+  if (a) cudaEventRecord(a, s);
+  cudaError_t e = launch();
+  if (b) cudaEventRecord(b, s);
+  if (a && b) h->prof.push_back(ProfRec{kind, a, b});
+  return e;
+}
 
 int check_shapes(int dtype, int d, int B) {
   if (B != 64 && B != 128) return 0;
@@ -265,6 +302,11 @@ int mf_bsr_create(mf_bsr_t* out, int n_layers, int T, int H_s, int B, int causal
 void mf_bsr_destroy(mf_bsr_t h) {
   if (!h) return;
   cudaDeviceSynchronize();
+  for (auto& r : h->prof) {
+    cudaEventDestroy(r.a);
+    cudaEventDestroy(r.b);
+  }
+  for (auto e : h->event_pool) cudaEventDestroy(e);
   for (auto& L : h->layers) release_layer(h, L, nullptr);
   dev_free(h, h->rbs_d, nullptr);
   dev_free(h, h->tiles_d, nullptr);
@@ -352,12 +394,15 @@ int mf_compress(mf_bsr_t h, int layer, const void* q, const void* k, int dtype, 
     if ((rc = make_map(&tq, q, (uint64_t)H_s * d, T, (uint64_t)H_s * d * 2, 64, 128)) != MF_OK) return rc;
     if ((rc = make_map(&tk, k, (uint64_t)H_ks * d, T, (uint64_t)H_ks * d * 2, 64, 128)) != MF_OK) return rc;
     if ((rc = make_map(&tk_pack, k, (uint64_t)H_ks * d, T, (uint64_t)H_ks * d * 2, 64, B)) != MF_OK) return rc;
-    MF_CUDA(launch_stats_bf16(cp, tq, tk, s), "statistics kernel");
+    MF_CUDA(timed(h, MF_K_STATS, s, [&] { return launch_stats_bf16(cp, tq, tk, s); }),
+            "statistics kernel");
   } else {
-    MF_CUDA(launch_stats_f32(cp, (const float*)q, (const float*)k, s), "statistics kernel (fp32)");
+    MF_CUDA(timed(h, MF_K_STATS, s,
+                  [&] { return launch_stats_f32(cp, (const float*)q, (const float*)k, s); }),
+            "statistics kernel (fp32)");
   }
-  MF_CUDA(launch_select(cp, s), "selection kernel");
-  MF_CUDA(launch_scan(cp, s), "row_ptr scan kernel");
+  MF_CUDA(timed(h, MF_K_SELECT, s, [&] { return launch_select(cp, s); }), "selection kernel");
+  MF_CUDA(timed(h, MF_K_SCAN, s, [&] { return launch_scan(cp, s); }), "row_ptr scan kernel");
   MF_CUDA(cudaMemcpyAsync(&h->host_pinned[0], L.nnz_dev, sizeof(long long), cudaMemcpyDeviceToHost, s),
           "nnz copy");
   MF_CUDA(cudaMemcpyAsync(&h->host_pinned[1], h->err_d, sizeof(int), cudaMemcpyDeviceToHost, s),
@@ -387,13 +432,16 @@ int mf_compress(mf_bsr_t h, int layer, const void* q, const void* k, int dtype, 
       if ((rc = make_map(&tvals, L.values, B, (uint64_t)nnz * B, (uint64_t)B * 2, 64,
                          B == 64 ? 64 : 128)) != MF_OK)
         return rc;
-      MF_CUDA(launch_pack_bf16(cp, tq, tk_pack, tvals, s), "pack kernel");
+      MF_CUDA(timed(h, MF_K_PACK, s, [&] { return launch_pack_bf16(cp, tq, tk_pack, tvals, s); }),
+              "pack kernel");
     }
   } else {
     if (nnz > 0)
-      MF_CUDA(launch_pack_f32(cp, (const float*)q, (const float*)k, L.values, s), "pack kernel (fp32)");
+      MF_CUDA(timed(h, MF_K_PACK, s,
+                    [&] { return launch_pack_f32(cp, (const float*)q, (const float*)k, L.values, s); }),
+              "pack kernel (fp32)");
   }
-  MF_CUDA(launch_union(cp, s), "union kernel");
+  MF_CUDA(timed(h, MF_K_UNION, s, [&] { return launch_union(cp, s); }), "union kernel");
   if (nnz > 0) {
     if ((rc = make_map(&L.pmap, L.values, B, (uint64_t)nnz * B, (uint64_t)B * 2, 64, 64)) != MF_OK)
       return rc;
@@ -457,9 +505,13 @@ int mf_retrieve(mf_bsr_t h, const float* W, const void* v, void* o, int dtype, i
       if (rc != MF_OK) return rc;
       CUtensorMap tp = L.pmap;
       if (L.nnz == 0) tp = tv;  // never dereferenced: no block-row has a kept tile
-      MF_CUDA(launch_retrieve_bf16(rp, tp, tv, ox, s), "retrieval kernel");
+      MF_CUDA(timed(h, MF_K_RETRIEVE, s, [&] { return launch_retrieve_bf16(rp, tp, tv, ox, s); }),
+              "retrieval kernel");
     } else {
-      MF_CUDA(launch_retrieve_f32(rp, L.values, (const float*)vx, (float*)ox, s),
+      MF_CUDA(timed(h, MF_K_RETRIEVE, s,
+                    [&] {
+                      return launch_retrieve_f32(rp, L.values, (const float*)vx, (float*)ox, s);
+                    }),
               "retrieval kernel (fp32)");
     }
   }
@@ -532,6 +584,36 @@ int mf_device_status(mf_bsr_t h, void* stream) {
     cudaStreamSynchronize(s);
     return fail(MF_ERR_TIMEOUT, "a device-side wait timed out");
   }
+  return MF_OK;
+}
+
+int mf_profile(mf_bsr_t h, int enable) {
+  if (!h) return fail(MF_ERR_ARG, "handle is NULL");
+  if (enable) {
+    for (auto& r : h->prof) {
+      h->event_pool.push_back(r.a);
+      h->event_pool.push_back(r.b);
+    }
+    h->prof.clear();
+    for (auto& c : h->launches) c = 0;
+  }
+  h->profiling = enable != 0;
+  return MF_OK;
+}
+
+int mf_profile_read(mf_bsr_t h, int kernel, int64_t* launches, double* total_ms) {
+  if (!h) return fail(MF_ERR_ARG, "handle is NULL");
+  if (kernel < 0 || kernel >= MF_K_COUNT) return fail(MF_ERR_ARG, "unknown kernel kind");
+  double tot = 0.0;
+  for (auto& r : h->prof) {
+    if (r.kind != kernel) continue;
+    MF_CUDA(cudaEventSynchronize(r.b), "event sync");
+    float ms = 0.f;
+    MF_CUDA(cudaEventElapsedTime(&ms, r.a, r.b), "event elapsed");
+    tot += ms;
+  }
+  if (launches) *launches = h->launches[kernel];
+  if (total_ms) *total_ms = tot;
   return MF_OK;
 }
 

@@ -21,7 +21,9 @@ MF_DTYPE_F32, MF_DTYPE_BF16 = 0, 1
 
 EXPORTED = ("mf_version", "mf_last_error", "mf_supported", "mf_bsr_create", "mf_bsr_destroy",
             "mf_compress", "mf_retrieve", "mf_bsr_info", "mf_bsr_export", "mf_bsr_copy",
-            "mf_bsr_release_layer", "mf_device_status", "mf_selftest_wait")
+            "mf_bsr_release_layer", "mf_device_status", "mf_selftest_wait", "mf_profile",
+            "mf_profile_read")
+KERNELS = ("stats", "select", "scan", "pack", "union", "retrieve")
 
 
 class MapFlowError(RuntimeError):
@@ -63,6 +65,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mf_bsr_release_layer.argtypes = [vp, i32]
     lib.mf_device_status.argtypes = [vp, vp]
     lib.mf_selftest_wait.argtypes = [vp, i32, vp]
+    lib.mf_profile.argtypes = [vp, i32]
+    lib.mf_profile_read.argtypes = [vp, i32, i64p, ctypes.POINTER(ctypes.c_double)]
     for name in EXPORTED:
         getattr(lib, name)
     _lib = lib
@@ -179,6 +183,16 @@ def mf_selftest_wait(h, limit_ms: int, stream=None) -> None:
     _check(load_library().mf_selftest_wait(h, int(limit_ms), _stream(stream)))
 
 
+def mf_profile(h, enable: bool) -> None:
+    _check(load_library().mf_profile(h, int(enable)))
+
+
+def mf_profile_read(h, kernel: int):
+    n, ms = ctypes.c_int64(), ctypes.c_double()
+    _check(load_library().mf_profile_read(h, kernel, ctypes.byref(n), ctypes.byref(ms)))
+    return n.value, ms.value
+
+
 # ------------------------------------------------------ convenience class --
 class BSR:
     """Owner of one mf_bsr_t (compressed sender state of several layers)."""
@@ -229,6 +243,13 @@ class BSR:
 
     def device_status(self, stream=None) -> None:
         mf_device_status(self.handle, stream)
+
+    def profile(self, enable: bool) -> None:
+        mf_profile(self.handle, enable)
+
+    def profile_read(self) -> Dict[str, tuple]:
+        """{kernel: (launches, total device ms)} since profiling was enabled."""
+        return {name: mf_profile_read(self.handle, i) for i, name in enumerate(KERNELS)}
 
     def close(self) -> None:
         if self.handle is not None:

@@ -213,6 +213,28 @@ MF_API int mf_bsr_release_layer(mf_bsr_t h, int layer);
  */
 MF_API int mf_device_status(mf_bsr_t h, void* stream);
 
+/* ---- per-kernel timing (CUDA events on the launching stream) ------------ */
+#define MF_K_STATS    0   /* compressor statistics (Q.K^T, row stats, masses) */
+#define MF_K_SELECT   1   /* block-level top-p                                */
+#define MF_K_SCAN     2   /* row_ptr scan                                     */
+#define MF_K_PACK     3   /* BSR pack (kept-tile recompute + store)           */
+#define MF_K_UNION    4   /* retrieval plan (union of kept columns)           */
+#define MF_K_RETRIEVE 5   /* fused retrieval                                  */
+#define MF_K_COUNT    6
+
+/*
+ * mf_profile — enable (1) or disable (0) event timing of every kernel the
+ * handle launches; enabling clears earlier records.  Launch counts are kept
+ * whether timing is on or not (reset by enabling).
+ */
+MF_API int mf_profile(mf_bsr_t h, int enable);
+
+/*
+ * mf_profile_read — launches and summed device time (ms) of one kernel kind
+ * since profiling was enabled.  Waits for the recorded events.
+ */
+MF_API int mf_profile_read(mf_bsr_t h, int kernel, int64_t* launches, double* total_ms);
+
 /*
  * mf_selftest_wait — failure-detection self-test (no counterpart on the
  * pages).  Launches one thread that waits on a device barrier nothing will

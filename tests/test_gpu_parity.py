@@ -66,11 +66,11 @@ def test_small_bf16(seqlens, Hs, Hks, d, B, Hr, Hkv):
 
 
 def test_noncausal():
-    small_case((190, 70), 2, 2, 128, 64, 4, 2, causal=False, structured=False)
+    small_case((190, 70), 2, 2, 128, 64, 0.9, 4, 2, causal=False, structured=False)
 
 
 def test_p1_keeps_every_block_with_mass():
-    ex = small_case((384,), 2, 2, 128, 64, 4, 2, p=1.0)
+    ex = small_case((384,), 2, 2, 128, 64, 1.0, 4, 2)
     # every causal candidate with non-zero fixed-point mass is kept
     assert ex["row_ptr"][-1] > 0
 
@@ -92,7 +92,7 @@ def test_nothing_kept_gives_zero_output():
 
 
 def test_unstructured_random_logits():
-    small_case((448,), 3, 3, 128, 64, 6, 3, p=0.9, structured=False, seed=7)
+    small_case((448,), 3, 3, 128, 64, 0.9, 6, 3, structured=False, seed=7)
 
 
 def test_fp32_workload0():
@@ -152,7 +152,7 @@ def test_device_wait_timeout_is_reported():
         bsr.device_status()
     assert ei.value.code == mapflow.MF_ERR_TIMEOUT
     bsr.device_status()  # cleared
-    small_case((128,), 1, 1, 64, 64, 1, 1)  # the context still works
+    small_case((128,), 1, 1, 64, 64, 0.9, 1, 1)  # the context still works
     bsr.close()
 
 
