@@ -1,0 +1,454 @@
+#!/usr/bin/env python
+"""Benchmark of the cross-model attention-map reuse hot path on one GB300.
+
+Workload (default): the 40-layer, 40-head sender (d = 128, bf16, N = 4096,
+B = 64, p = 0.95) feeding a 36-layer receiver with 32 query / 8 KV heads that
+recomputes its first 4 layers and reuses layers 5..36 through
+m(j) = round(j * 40 / 36).  One step = the whole hot path over one batch:
+compress all 40 sender layers (statistics, top-p, BSR pack) and run the
+fused retrieval for the 32 reuse layers.  Inputs are seeded synthetic tensors
+(no model weights or datasets), resident in HBM before the timed region.
+
+Printed JSON (one line, rank 0):
+  value       retrieval GB/s: algorithmic bytes of the 32 retrieval launches
+              per step / their device time (CUDA events), summed over ranks
+  compressor  tokens/s of the compressor and its Q.K^T tensor fraction
+  roofline    the dominant kernel (largest device time in the step) against
+              MEASURED_PEAKS.json; `rooflines` has all three hot kernels
+  e2e         the same metric through the public API with host buffers:
+              host->device copies of every input and device->host read of O
+              inside the timed region
+  cpu_baseline  the fp64 oracle on a bounded sample, host cores
+
+`--impl reference` times the oracle itself as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import multiprocessing as mp
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from cross_model_attention_gb300 import synth, workloads  # noqa: E402
+
+METRIC = "retrieval GB/s & % HBM roofline; compressor tokens/s & % tensor peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ------------------------------------------------------------ workload ----
+
+def _gen_layer(args):
+    widx, layer = args
+    w = workloads.get(widx)
+    q, k = synth.sender_qk_f32(w, layer)
+    return synth.bf16_round(q), synth.bf16_round(k)
+
+
+def generate_inputs(widx: int, procs: int):
+    """Seeded host inputs; generated in a spawn pool before any CUDA call."""
+    w = workloads.get(widx)
+    rcv = w.receivers[0]
+    lm = rcv.layer_map(w.sender_layers)
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(max(1, procs)) as pool:
+        qk = pool.map(_gen_layer, [(widx, l) for l in range(1, w.sender_layers + 1)])
+    v = np.stack([synth.receiver_v(w, rcv, j)["v"] for j, _ in lm])
+    W = np.stack([synth.head_map_weights(w, rcv, j) for j, _ in lm])
+    return w, rcv, lm, qk, v, W
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            pk = json.load(fh)
+        return pk, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def qk_flops(w) -> float:
+    """Q.K^T flops of one causal pass over one sender layer."""
+    return float(sum(2.0 * w.d * w.sender_heads * L * (L + 1) / 2 for L in w.seqlens))
+
+
+def retrieval_bytes(w, rcv, nnz: int) -> float:
+    """Algorithmic HBM bytes of one retrieval launch (one reuse layer)."""
+    R = sum((L + w.B - 1) // w.B for L in w.seqlens)
+    return float(nnz * 2 * w.B * w.B + 4 * nnz + 4 * (w.sender_heads * R + 1)
+                 + 4 * rcv.heads * w.sender_heads + 2 * w.T * rcv.kv_heads * w.d
+                 + 2 * w.T * rcv.heads * w.d)
+
+
+def pack_bytes(w, nnz: int) -> float:
+    """Algorithmic HBM bytes of one pack launch: Q and K read once, kept tiles
+    and col_idx written."""
+    return float(2 * w.T * (w.sender_heads + w.sender_kv_heads) * w.d + nnz * 2 * w.B * w.B
+                 + 4 * nnz)
+
+
+def traffic_for(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current source of that kernel; else None."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    src = {"stats": "mf_stats_tc.cu", "pack": "mf_pack_tc.cu", "retrieve": "mf_retrieve_tc.cu"}[kernel]
+    with open(os.path.join(ROOT, "cross_model_attention_gb300", "csrc", src), "rb") as fh:
+        sha = hashlib.sha256(fh.read()).hexdigest()[:16]
+    if not os.path.exists(path):
+        return None
+    for line in open(path):
+        parts = line.split()
+        if len(parts) >= 3 and parts[0] == kernel and parts[1] == sha:
+            return float(parts[2])
+    return None
+
+
+# -------------------------------------------------------------- clocks ----
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int = 0):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[2:6]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------ CPU leg ----
+
+def oracle_sample(w, rcv, qk, v, W, lm, budget_rows: int = 6, heads: int = 2, seed: int = 0):
+    """Time the oracle on a bounded sample of the workload: the compressor on
+    `heads` heads of one sender layer, and the retrieval of `budget_rows`
+    block-rows of one reuse layer.  Returns per-unit throughputs."""
+    from oracle import mapflow_oracle as orc
+    layer = lm[0][1]
+    q64 = synth.bf16_to_f64(qk[layer - 1][0])
+    k64 = synth.bf16_to_f64(qk[layer - 1][1])
+    t0 = time.perf_counter()
+    bsr = orc.compress(q64[:, :heads], k64[:, :heads], w.cu_seqlens, w.B, w.p[0], True,
+                       keep_tiles=False)
+    t_comp = time.perf_counter() - t0
+    grid = bsr.grid
+    rng = np.random.default_rng(seed)
+    rows = sorted(int(x) for x in rng.choice(grid.R, size=min(budget_rows, grid.R), replace=False))
+    # kept sets of every head for the sampled rows (the oracle's own selection)
+    kept = {}
+    for h in range(w.sender_heads):
+        for rb in rows:
+            ref = orc.block_row_reference(q64, k64, grid, h, rb)
+            kept[(h, rb)] = orc.select_topp(ref["mass"], w.p[0])
+    v64 = synth.bf16_to_f64(v[0])
+    t0 = time.perf_counter()
+    nbytes = 0.0
+    for rb in rows:
+        orc.retrieve_block_row(q64, k64, grid, lambda h, r: kept[(h, r)], W[0].astype(np.float64),
+                               v64, rcv.kv_heads, rb)
+        nk = sum(len(kept[(h, rb)]) for h in range(w.sender_heads))
+        nrow = min(w.B, int(grid.lens[grid.rb_seq[rb]]) - int(grid.rb_local[rb]) * w.B)
+        nbytes += nk * (2 * w.B * w.B + 4) + 2 * nrow * (rcv.heads + rcv.kv_heads) * w.d
+    t_ret = time.perf_counter() - t0
+    return {
+        "retrieval_gbs": nbytes / t_ret / 1e9,
+        "compressor_tokens_per_s": w.T * heads / w.sender_heads / t_comp,
+        "seconds": t_comp + t_ret,
+        "sample": (f"oracle compressor on {heads}/{w.sender_heads} heads of sender layer {layer} "
+                   f"(N={w.T}); oracle retrieval of {len(rows)}/{grid.R} block-rows of reuse "
+                   f"layer {lm[0][0]} (all {w.sender_heads} sender heads, {rcv.heads} receiver "
+                   f"heads)"),
+    }
+
+
+def run_reference(args, rank: int, world: int):
+    if rank != 0:
+        return
+    w, rcv, lm, qk, v, W = generate_inputs(args.workload, args.procs)
+    for _ in range(args.warmup):
+        oracle_sample(w, rcv, qk, v, W, lm, budget_rows=args.ref_rows, heads=1)
+    vals, comps, secs = [], [], []
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        r = oracle_sample(w, rcv, qk, v, W, lm, budget_rows=args.ref_rows, heads=1, seed=i)
+        vals.append(r["retrieval_gbs"])
+        comps.append(r["compressor_tokens_per_s"])
+        secs.append(r["seconds"])
+        sample = r["sample"]
+    wall = time.perf_counter() - t0
+    value = statistics.median(vals)
+    cores = os.cpu_count()
+    out = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * wall / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_dict(w, rcv, world),
+        "compressor": {"tokens_per_s": statistics.median(comps)},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def config_dict(w, rcv, world):
+    return {"workload": f"workload {w.index}: {w.name}", "sender_layers": w.sender_layers,
+            "sender_heads": w.sender_heads, "sender_kv_heads": w.sender_kv_heads,
+            "receiver_layers": rcv.layers, "receiver_heads": rcv.heads,
+            "receiver_kv_heads": rcv.kv_heads, "recompute_r": rcv.recompute,
+            "reuse_layers": rcv.layers - rcv.recompute, "N": w.T, "d": w.d, "B": w.B,
+            "p": w.p[0], "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+            "l2": "inputs larger than L2 (per-layer BSR ~0.65 GB, Q/K of 40 layers 3.4 GB)"}
+
+
+# ------------------------------------------------------------ GPU leg ----
+
+def run_gpu(args, rank: int, world: int, local_rank: int):
+    w, rcv, lm, qk, v, W = generate_inputs(args.workload, args.procs)
+    import torch
+    import torch.distributed as dist
+    from cross_model_attention_gb300 import mapflow
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    Ls, T, Hs, Hks, d = w.sender_layers, w.T, w.sender_heads, w.sender_kv_heads, w.d
+    n_r = len(lm)
+    layer_map = [m - 1 for _, m in lm]
+
+    def to_bf16(a):
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+
+    q_h = torch.stack([to_bf16(x[0]) for x in qk]).pin_memory()
+    k_h = torch.stack([to_bf16(x[1]) for x in qk]).pin_memory()
+    v_h = to_bf16(v).pin_memory()
+    W_h = torch.from_numpy(W).pin_memory()
+    q_d, k_d = q_h.to(dev), k_h.to(dev)
+    v_d, W_d = v_h.to(dev), W_h.to(dev)
+    o_d = torch.empty((n_r, T, rcv.heads, d), dtype=torch.bfloat16, device=dev)
+    o_h = torch.empty(o_d.shape, dtype=torch.bfloat16).pin_memory()
+    stream = torch.cuda.current_stream()
+    bsr = mapflow.BSR(Ls, T, Hs, w.B, w.cu_seqlens)
+
+    def compress_all():
+        for l in range(Ls):
+            bsr.compress(l, q_d[l], k_d[l], w.p[0])
+
+    def retrieve_all():
+        bsr.retrieve(W_d, v_d, o_d, layer_map)
+
+    for _ in range(args.warmup):
+        compress_all()
+        retrieve_all()
+    bsr.device_status()
+    nnz = [bsr.info(l)[0] for l in range(Ls)]
+    ret_bytes = sum(retrieval_bytes(w, rcv, nnz[m]) for m in layer_map)
+    comp_flops = qk_flops(w) * Ls
+    pk_bytes = sum(pack_bytes(w, n) for n in nnz)
+
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    bsr.profile(True)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    t_wall0 = time.perf_counter()
+    for i in range(args.steps):
+        evs[i][0].record(stream)
+        compress_all()
+        evs[i][1].record(stream)
+        retrieve_all()
+        evs[i][2].record(stream)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    bsr.device_status()
+    prof = bsr.profile_read()
+    bsr.profile(False)
+    t_comp = sum(e[0].elapsed_time(e[1]) for e in evs) / 1e3
+    t_ret = sum(e[1].elapsed_time(e[2]) for e in evs) / 1e3
+    t_step = evs[0][0].elapsed_time(evs[-1][2]) / 1e3
+    times = torch.tensor([t_step, t_comp, t_ret], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(times, op=dist.ReduceOp.MAX)
+    t_step, t_comp, t_ret = times.tolist()
+    K = args.steps
+    value = ret_bytes * K * world / t_ret / 1e9
+    comp_tps = T * Ls * K * world / t_comp
+
+    peaks, src = load_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    tf_sus = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
+    label = "of measured" if src == "measured" else "of fallback"
+
+    def roof(kind):
+        n, ms = prof[kind]
+        per = ms / max(n, 1) / 1e3
+        if kind == "stats":
+            ach = comp_flops / Ls / per / 1e12
+            return {"bound": "tensor", "achieved": ach, "peak": tf_sus, "unit": "TFLOP/s",
+                    "frac": ach / tf_sus, "traffic": traffic_for("stats"), "launches": n,
+                    "ms_per_launch": per * 1e3, "peak_source": f"bf16_tflops_sustained ({label})"}
+        if kind == "pack":
+            ach = pk_bytes / Ls / per / 1e9
+        else:
+            ach = ret_bytes / n_r / per / 1e9
+        return {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+                "traffic": traffic_for(kind), "launches": n, "ms_per_launch": per * 1e3,
+                "frac_of_8TBs_nominal": ach / 8000.0, "peak_source": f"hbm_gbs ({label})"}
+
+    rooflines = {k: roof(k) for k in ("stats", "pack", "retrieve")}
+    dominant = max(("stats", "pack", "retrieve"), key=lambda k: prof[k][1])
+    launches = sum(n for n, _ in prof.values())
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        reps = max(1, min(2, K))
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        tc, tr = 0.0, 0.0
+        for _ in range(reps):
+            ev[0].record(stream)
+            for l in range(Ls):
+                q_d[l].copy_(q_h[l], non_blocking=True)
+                k_d[l].copy_(k_h[l], non_blocking=True)
+                bsr.compress(l, q_d[l], k_d[l], w.p[0])
+            ev[1].record(stream)
+            ev[2].record(stream)
+            v_d.copy_(v_h, non_blocking=True)
+            W_d.copy_(W_h, non_blocking=True)
+            retrieve_all()
+            o_h.copy_(o_d, non_blocking=True)
+            ev[3].record(stream)
+            torch.cuda.synchronize()
+            tc += ev[0].elapsed_time(ev[1]) / 1e3
+            tr += ev[2].elapsed_time(ev[3]) / 1e3
+        h2d = (q_h.numel() + k_h.numel() + v_h.numel()) * 2 + W_h.numel() * 4
+        e2e = {"value": ret_bytes * reps * world / tr / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(o_h.numel() * 2 + 16 * Ls),
+               "compressor_tokens_per_s": T * Ls * reps * world / tc}
+
+    bsr.close()
+    out = None
+    if rank == 0:
+        cpu = None
+        if world == 1 and not args.no_cpu_baseline:
+            r = oracle_sample(w, rcv, qk, v, W, lm, budget_rows=args.cpu_rows, heads=args.cpu_heads)
+            cpu = {"value": r["retrieval_gbs"], "unit": "GB/s", "cores": os.cpu_count(),
+                   "kind": "oracle", "sample": r["sample"],
+                   "compressor_tokens_per_s": r["compressor_tokens_per_s"],
+                   "seconds": r["seconds"],
+                   "threads_note": "numpy BLAS matmul on all host cores; elementwise ops on one"}
+        out = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": 1e3 * t_step / K, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": config_dict(w, rcv, world),
+            "compressor": {"tokens_per_s": comp_tps,
+                           "qk_tensor_frac": rooflines["stats"]["frac"],
+                           "qk_tflops": rooflines["stats"]["achieved"],
+                           "ms_per_step": 1e3 * t_comp / K},
+            "retrieval": {"ms_per_step": 1e3 * t_ret / K, "bytes_per_step": ret_bytes,
+                          "hbm_frac": rooflines["retrieve"]["frac"],
+                          "kept_fraction": float(np.mean(nnz)) / (Hs * sum(
+                              (L + w.B - 1) // w.B * ((L + w.B - 1) // w.B + 1) // 2
+                              for L in w.seqlens))},
+            "roofline": rooflines[dominant] | {"kernel": dominant},
+            "rooflines": rooflines,
+            "gpu_launches": launches,
+            "clocks": clk,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+            "wall_s_timed": t_wall,
+        }
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", type=int, default=1)
+    ap.add_argument("--procs", type=int, default=min(16, os.cpu_count() or 4))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-rows", type=int, default=16)
+    ap.add_argument("--cpu-heads", type=int, default=2)
+    ap.add_argument("--ref-rows", type=int, default=3)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_gpu(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

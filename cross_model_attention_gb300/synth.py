@@ -42,9 +42,13 @@ SINK_KEYS = 4
 def bf16_round(x: np.ndarray) -> np.ndarray:
     """Round fp32 values to bf16 (nearest-even); returns uint16 bit patterns."""
     x = np.ascontiguousarray(x, dtype=np.float32)
-    b = x.view(np.uint32).astype(np.uint64)
-    b = (b + 0x7FFF + ((b >> 16) & 1)) >> 16
-    return b.astype(np.uint16)
+    b = x.view(np.uint32)
+    # finite inputs only: b + 0x8000 never wraps a 32-bit word
+    r = (b >> 16) & np.uint32(1)
+    r += np.uint32(0x7FFF)
+    r += b
+    r >>= 16
+    return r.astype(np.uint16)
 
 
 def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
@@ -80,7 +84,6 @@ def sender_qk_f32(w: Workload, layer: int) -> Tuple[np.ndarray, np.ndarray]:
     omega = rng.uniform(0.0, math.pi / 32.0, size=BAND_PAIRS)
     c = math.sqrt(2.0 / BAND_PAIRS)
     cu = w.cu_seqlens
-    nblk_ret = []
     for s in range(len(w.seqlens)):
         a, b = int(cu[s]), int(cu[s + 1])
         L = b - a
@@ -102,7 +105,6 @@ def sender_qk_f32(w: Workload, layer: int) -> Tuple[np.ndarray, np.ndarray]:
             for hk in range(Hks):
                 pick = rng.choice(np.arange(1, nb), size=min(w.retrieval_blocks, nb - 1),
                                   replace=False)
-                nblk_ret.append(pick)
                 for bj in pick:
                     k[a + bj * w.B:a + min(L, (bj + 1) * w.B), hk, col] = 3.0 * sd
     if w.temperature is not None:
