@@ -617,6 +617,47 @@ int mf_profile_read(mf_bsr_t h, int kernel, int64_t* launches, double* total_ms)
   return MF_OK;
 }
 
+int mf_select_noalloc(const float* mass, const int32_t* cu_seqlens_host, int n_seqs, int H_s,
+                      int B, int causal, float p, int32_t* row_ptr, int32_t* col_idx,
+                      int64_t col_capacity, int64_t* nnz, void* stream) {
+  if (!mass || !cu_seqlens_host || !row_ptr || !col_idx || !nnz)
+    return fail(MF_ERR_ARG, "NULL pointer argument");
+  if (n_seqs < 1 || H_s < 1) return fail(MF_ERR_ARG, "n_seqs and H_s must be >= 1");
+  if (B != 64 && B != 128) return fail(MF_ERR_UNSUPPORTED, "block size %d (supported: 64, 128)", B);
+  if (causal != 0 && causal != 1) return fail(MF_ERR_ARG, "causal must be 0 or 1");
+  if (!(p > 0.f && p <= 1.f)) return fail(MF_ERR_ARG, "p must be in (0, 1]");
+  if (cu_seqlens_host[0] != 0) return fail(MF_ERR_ARG, "cu_seqlens[0] must be 0");
+  std::vector<RowBlock> rbs;
+  long long cand = 0;
+  for (int s = 0; s < n_seqs; ++s) {
+    const int start = cu_seqlens_host[s], L = cu_seqlens_host[s + 1] - cu_seqlens_host[s];
+    if (L < 0) return fail(MF_ERR_ARG, "cu_seqlens must be non-decreasing (sequence %d)", s);
+    if (L > 256 * B)
+      return fail(MF_ERR_UNSUPPORTED, "sequence %d has length %d > 256*B = %d", s, L, 256 * B);
+    const int nb = (L + B - 1) / B;
+    for (int bi = 0; bi < nb; ++bi) {
+      rbs.push_back(RowBlock{start, L, bi, (int)cand});
+      cand += causal ? bi + 1 : nb;
+    }
+  }
+  const long long R = (long long)rbs.size();
+  if (R == 0) return fail(MF_ERR_ARG, "no tokens");
+  if (col_capacity < (long long)H_s * cand)
+    return fail(MF_ERR_ARG, "col_capacity %lld < H_s * candidates = %lld",
+                (long long)col_capacity, (long long)H_s * cand);
+  const size_t need = noalloc_needed_bytes(R, H_s, cand);
+  if (need > noalloc_scratch_bytes())
+    return fail(MF_ERR_UNSUPPORTED,
+                "this selection needs %zu bytes of scratch; the no-allocation entry point "
+                "reserves %zu bytes per device",
+                need, noalloc_scratch_bytes());
+  MF_CUDA(launch_select_noalloc(rbs.data(), (int)R, (int)cand, H_s, B, causal, p, mass, row_ptr,
+                                col_idx, reinterpret_cast<long long*>(nnz),
+                                static_cast<cudaStream_t>(stream)),
+          "no-allocation selection");
+  return MF_OK;
+}
+
 int mf_selftest_wait(mf_bsr_t h, int limit_ms, void* stream) {
   if (!h) return fail(MF_ERR_ARG, "handle is NULL");
   if (limit_ms < 1 || limit_ms > 10000) return fail(MF_ERR_ARG, "limit_ms must be in [1, 10000]");

@@ -85,6 +85,13 @@ cudaError_t launch_retrieve_bf16(const RetrieveParams& p, const CUtensorMap& tp,
 cudaError_t launch_retrieve_f32(const RetrieveParams& p, const uint16_t* values, const float* v,
                                 float* o, cudaStream_t s);
 
+// No-allocation selection (scratch in a static device array; mf_noalloc.cu).
+size_t noalloc_scratch_bytes();
+size_t noalloc_needed_bytes(long long R, long long H_s, long long C);
+cudaError_t launch_select_noalloc(const RowBlock* rbs_host, int R, int C, int H_s, int B,
+                                  int causal, float p, const float* mass, int* row_ptr,
+                                  int* col_idx, long long* nnz, cudaStream_t s);
+
 cudaError_t launch_selftest_wait(int* err, unsigned long long limit_ns, cudaStream_t s);
 
 }  // namespace mf

@@ -22,7 +22,7 @@ MF_DTYPE_F32, MF_DTYPE_BF16 = 0, 1
 EXPORTED = ("mf_version", "mf_last_error", "mf_supported", "mf_bsr_create", "mf_bsr_destroy",
             "mf_compress", "mf_retrieve", "mf_bsr_info", "mf_bsr_export", "mf_bsr_copy",
             "mf_bsr_release_layer", "mf_device_status", "mf_selftest_wait", "mf_profile",
-            "mf_profile_read")
+            "mf_profile_read", "mf_select_noalloc")
 KERNELS = ("stats", "select", "scan", "pack", "union", "retrieve")
 
 
@@ -65,6 +65,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mf_bsr_release_layer.argtypes = [vp, i32]
     lib.mf_device_status.argtypes = [vp, vp]
     lib.mf_selftest_wait.argtypes = [vp, i32, vp]
+    lib.mf_select_noalloc.argtypes = [vp, ctypes.POINTER(ctypes.c_int32), i32, i32, i32, i32,
+                                      ctypes.c_float, vp, vp, ctypes.c_int64, vp, vp]
     lib.mf_profile.argtypes = [vp, i32]
     lib.mf_profile_read.argtypes = [vp, i32, i64p, ctypes.POINTER(ctypes.c_double)]
     for name in EXPORTED:
@@ -181,6 +183,16 @@ def mf_device_status(h, stream=None) -> None:
 
 def mf_selftest_wait(h, limit_ms: int, stream=None) -> None:
     _check(load_library().mf_selftest_wait(h, int(limit_ms), _stream(stream)))
+
+
+def mf_select_noalloc(mass, cu_seqlens: Sequence[int], H_s: int, B: int, causal: bool,
+                      p: float, row_ptr, col_idx, nnz, stream=None) -> None:
+    """Selection into caller buffers with no device allocation (see mapflow.h)."""
+    cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
+    _check(load_library().mf_select_noalloc(
+        _ptr(mass), cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), len(cu) - 1, H_s, B,
+        int(causal), float(p), _ptr(row_ptr), _ptr(col_idx), int(col_idx.numel()), _ptr(nnz),
+        _stream(stream)))
 
 
 def mf_profile(h, enable: bool) -> None:

@@ -236,6 +236,40 @@ MF_API int mf_profile(mf_bsr_t h, int enable);
 MF_API int mf_profile_read(mf_bsr_t h, int kernel, int64_t* launches, double* total_ms);
 
 /*
+ * mf_select_noalloc — block-level top-p selection and BSR structure from a
+ * caller's block masses, allocating NO device memory.  The pages have no
+ * counterpart of this call: it exists for callers that cannot allocate when
+ * they select — engines that reserve almost all device memory up front and
+ * forbid further cudaMalloc, code inside CUDA stream capture (where
+ * cudaMalloc/cudaFree are illegal), and latency-critical loops that cannot
+ * pay cudaFree's implicit device synchronisation.
+ *
+ *   mass             fp32 [H_s][C] candidate masses in mf_bsr_export's layout
+ *                    (input; e.g. exported from mf_compress)
+ *   cu_seqlens_host  HOST int32 [n_seqs+1] (as for mf_bsr_create)
+ *   H_s, B, causal, p  as for mf_compress
+ *   row_ptr          int32 [H_s*R + 1] output
+ *   col_idx          int32 output with room for col_capacity entries;
+ *                    col_capacity must be >= H_s*C (every candidate kept)
+ *   nnz              DEVICE int64 output: number of kept tiles
+ *
+ * The selection rule and the output are exactly mf_compress's row_ptr and
+ * col_idx for the same masses.  Intermediates live in one file-scope static
+ * device array of 16 MiB per device (held by every GPU that loads the
+ * library until the process exits); a call needing more is rejected with
+ * MF_ERR_UNSUPPORTED.  The first call on each device looks up that array's
+ * device address (cudaGetSymbolAddress) — make that first call before any
+ * stream capture.  All calls on a device share the array: calls that overlap
+ * on the GPU (different streams without ordering) race; calls ordered on one
+ * stream are safe.  Nothing needs clearing between calls.  The host table of
+ * block-rows is copied to the device before the call returns; the kernels
+ * run asynchronously on `stream`.
+ */
+MF_API int mf_select_noalloc(const float* mass, const int32_t* cu_seqlens_host, int n_seqs,
+                             int H_s, int B, int causal, float p, int32_t* row_ptr,
+                             int32_t* col_idx, int64_t col_capacity, int64_t* nnz, void* stream);
+
+/*
  * mf_selftest_wait — failure-detection self-test (no counterpart on the
  * pages).  Launches one thread that waits on a device barrier nothing will
  * complete, bounded by `limit_ms` milliseconds (1..10000); the wait gives up,
