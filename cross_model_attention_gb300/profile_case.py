@@ -1,0 +1,70 @@
+"""A small case of the hot path for kernel profiling (ncu) and quick timing.
+
+Runs `--layers` sender layers of a workload through mf_compress and the same
+number of receiver layers through mf_retrieve, at the workload's real
+per-layer sizes (so one launch moves exactly the bytes of one bench launch),
+while keeping the device footprint to a few GB.  Prints per-kernel launch
+counts and mean device times from the library's event profiler.
+
+    python -m cross_model_attention_gb300.profile_case --workload 1 --layers 2
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import sys
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--workload", type=int, default=1)
+    ap.add_argument("--layers", type=int, default=2)
+    ap.add_argument("--repeat", type=int, default=2)
+    ap.add_argument("--p", type=float, default=None)
+    args = ap.parse_args()
+
+    from cross_model_attention_gb300 import synth, workloads
+    w = workloads.get(args.workload)
+    rcv = w.receivers[0]
+    lm = rcv.layer_map(w.sender_layers)[:args.layers]
+    p = w.p[0] if args.p is None else args.p
+    qk = [synth.sender_qk(w, m) for _, m in lm]
+    vs = np.stack([synth.receiver_v(w, rcv, j)["v"] for j, _ in lm])
+    Ws = np.stack([synth.head_map_weights(w, rcv, j) for j, _ in lm])
+
+    import torch
+    import __graft_entry__
+    from cross_model_attention_gb300 import mapflow
+    __graft_entry__.build()
+    dev = torch.device("cuda", 0)
+    conv = (lambda a: torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)) \
+        if w.dtype == "bf16" else (lambda a: torch.from_numpy(a).to(dev))
+    q = [conv(x["q"]) for x in qk]
+    k = [conv(x["k"]) for x in qk]
+    v = conv(vs)
+    W = torch.from_numpy(Ws).to(dev)
+    o = torch.empty((len(lm), w.T, rcv.heads, w.d), dtype=v.dtype, device=dev)
+    bsr = mapflow.BSR(len(lm), w.T, w.sender_heads, w.B, w.cu_seqlens)
+    bsr.profile(True)
+    for _ in range(args.repeat):
+        for l in range(len(lm)):
+            bsr.compress(l, q[l], k[l], p)
+        bsr.retrieve(W, v, o, list(range(len(lm))))
+    bsr.device_status()
+    prof = bsr.profile_read()
+    out = {name: {"launches": n, "ms_per_launch": (ms / n if n else None)}
+           for name, (n, ms) in prof.items()}
+    out["nnz"] = [bsr.info(l)[0] for l in range(len(lm))]
+    print(json.dumps(out))
+    bsr.close()
+
+
+if __name__ == "__main__":
+    main()
