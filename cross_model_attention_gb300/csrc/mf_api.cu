@@ -99,7 +99,8 @@ struct LayerState {
   int* col_idx = nullptr;
   uint16_t* values = nullptr;
   size_t values_bytes = 0, colidx_bytes = 0;
-  CUtensorMap pmap;  // values as [nnz*B rows][B cols], 64x64 boxes (retrieval)
+  CUtensorMap pmap;  // values as [(nnz+1)*B rows][B cols], 64x64 boxes (per-group retrieval)
+  CUtensorMap gmap;  // same rows, 64x1 boxes for 4-row gathers (cluster retrieval)
 };
 
 struct ProfRec {
@@ -418,7 +419,9 @@ int mf_compress(mf_bsr_t h, int layer, const void* q, const void* k, int dtype, 
   L.nnz = nnz;
   L.values_bytes = (size_t)nnz * B * B * 2;
   L.colidx_bytes = (size_t)nnz * 4;
-  L.values = (uint16_t*)dev_alloc(h, L.values_bytes, s);
+  // one extra all-zero tile after the kept ones: the retrieval reads it in
+  // place of a head's dropped block
+  L.values = (uint16_t*)dev_alloc(h, L.values_bytes + (size_t)B * B * 2, s);
   L.col_idx = (int*)dev_alloc(h, L.colidx_bytes, s);
   if (!L.values || !L.col_idx) {
     release_layer(h, L, s);
@@ -426,6 +429,8 @@ int mf_compress(mf_bsr_t h, int layer, const void* q, const void* k, int dtype, 
   }
   cp.col_idx = L.col_idx;
   MF_CUDA(cudaMemsetAsync(L.tile_of, 0xFF, HC * 4, s), "tile index reset");
+  MF_CUDA(cudaMemsetAsync(reinterpret_cast<char*>(L.values) + L.values_bytes, 0, (size_t)B * B * 2, s),
+          "zero tile");
   if (dtype == MF_DTYPE_BF16) {
     CUtensorMap tvals{};
     if (nnz > 0) {
@@ -442,10 +447,10 @@ int mf_compress(mf_bsr_t h, int layer, const void* q, const void* k, int dtype, 
               "pack kernel (fp32)");
   }
   MF_CUDA(timed(h, MF_K_UNION, s, [&] { return launch_union(cp, s); }), "union kernel");
-  if (nnz > 0) {
-    if ((rc = make_map(&L.pmap, L.values, B, (uint64_t)nnz * B, (uint64_t)B * 2, 64, 64)) != MF_OK)
-      return rc;
-  }
+  if ((rc = make_map(&L.pmap, L.values, B, (uint64_t)(nnz + 1) * B, (uint64_t)B * 2, 64, 64)) != MF_OK)
+    return rc;
+  if ((rc = make_map(&L.gmap, L.values, B, (uint64_t)(nnz + 1) * B, (uint64_t)B * 2, 64, 1)) != MF_OK)
+    return rc;
   L.valid = true;
   L.dtype = dtype;
   L.d = d;
@@ -496,6 +501,7 @@ int mf_retrieve(mf_bsr_t h, const float* W, const void* v, void* o, int dtype, i
     rp.union_cnt = L.union_cnt;
     rp.union_list = L.union_list;
     rp.W = W + (size_t)x * H_r * h->H_s;
+    rp.zero_tile = (int)L.nnz;
     rp.err = h->err_d;
     const char* vx = static_cast<const char*>(v) + x * v_layer;
     char* ox = static_cast<char*>(o) + x * o_layer;
@@ -503,10 +509,15 @@ int mf_retrieve(mf_bsr_t h, const float* W, const void* v, void* o, int dtype, i
       CUtensorMap tv{};
       int rc = make_map(&tv, vx, (uint64_t)H_kv * d, h->T, (uint64_t)H_kv * d * 2, 64, 64);
       if (rc != MF_OK) return rc;
-      CUtensorMap tp = L.pmap;
-      if (L.nnz == 0) tp = tv;  // never dereferenced: no block-row has a kept tile
-      MF_CUDA(timed(h, MF_K_RETRIEVE, s, [&] { return launch_retrieve_bf16(rp, tp, tv, ox, s); }),
-              "retrieval kernel");
+      if (retrieve_cluster_supported(h->H_s, H_r, H_kv, d, h->B)) {
+        MF_CUDA(timed(h, MF_K_RETRIEVE, s,
+                      [&] { return launch_retrieve_cluster(rp, L.gmap, tv, ox, s); }),
+                "retrieval kernel (cluster)");
+      } else {
+        MF_CUDA(timed(h, MF_K_RETRIEVE, s,
+                      [&] { return launch_retrieve_bf16(rp, L.pmap, tv, ox, s); }),
+                "retrieval kernel");
+      }
     } else {
       MF_CUDA(timed(h, MF_K_RETRIEVE, s,
                     [&] {

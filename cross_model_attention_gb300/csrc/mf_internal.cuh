@@ -63,6 +63,7 @@ struct RetrieveParams {
   const int* union_cnt;   // [R]
   const int* union_list;  // [C]
   const float* W;         // [H_r][H_s] of this receiver layer
+  int zero_tile;          // index of an all-zero tile (= nnz)
   int* err;
 };
 
@@ -82,6 +83,9 @@ cudaError_t launch_pack_f32(const CompressParams& p, const float* q, const float
 cudaError_t launch_union(const CompressParams& p, cudaStream_t s);
 cudaError_t launch_retrieve_bf16(const RetrieveParams& p, const CUtensorMap& tp,
                                  const CUtensorMap& tv, void* o, cudaStream_t s);
+bool retrieve_cluster_supported(int H_s, int H_r, int H_kv, int d, int B);
+cudaError_t launch_retrieve_cluster(const RetrieveParams& p, const CUtensorMap& tp,
+                                    const CUtensorMap& tv, void* o, cudaStream_t s);
 cudaError_t launch_retrieve_f32(const RetrieveParams& p, const uint16_t* values, const float* v,
                                 float* o, cudaStream_t s);
 

@@ -31,8 +31,8 @@ struct PackLayout {
   static constexpr int kQBytes = kRows * D * 2;
   static constexpr int kKChunk = BLK * 128;            // BLK key rows x 64 bf16
   static constexpr int kKBytes = BLK * D * 2;
-  static constexpr int kStages = 3;
-  static constexpr int kStageBytes = (BLK == 64) ? 2 * 64 * 128 : 2 * 128 * 128;  // staging
+  static constexpr int kStages = 2;  // keeps two CTAs per SM at B = 64
+  static constexpr int kStageBytes = 2 * ((BLK == 64) ? 2 * 64 * 128 : 2 * 128 * 128);  // 2 staging buffers
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + kQBytes;
   static constexpr int kStg = kK + kStages * kKBytes;
@@ -223,6 +223,7 @@ __global__ void __launch_bounds__(192, 1)
     const int grp_threads = (BLK == 64) ? 64 : 128;
     const int bar_id = (BLK == 64) ? 2 + sub : 2;
     const bool leader = (BLK == 64) ? (rloc == 0) : (row == 0);
+    int nstore = 0;
     for (int u = 0; u < n_u; ++u) {
       const int b = u & 1;
       if (!warp_wait(barSFull(b), (u >> 1) & 1, p.err)) break;
@@ -240,38 +241,51 @@ __global__ void __launch_bounds__(192, 1)
       const int pos = (sub == 0) ? u_pos0[u] : u_pos1[u];
       if (pos < 0) continue;  // this block-row does not keep the block (group-uniform)
       const int bj = u_bj[u];
-      // wait until the previous store has finished reading the staging tile
-      if (leader) bulk_wait_read_all();
+      const int sbuf = nstore & 1;
+      ++nstore;
+      // the store issued from this staging buffer two tiles ago must have
+      // finished reading it
+      if (leader) bulk_wait_read_1();
       named_bar(bar_id, grp_threads);
+      // only the diagonal block and the sequence's last block need masking
+      const bool edge = !row_ok || (bj * BLK + BLK > tile.L) ||
+                        (p.causal && bj * BLK + BLK - 1 > tile.tl * kRows + (row - rloc));
 #pragma unroll
       for (int c8 = 0; c8 < BLK / 8; ++c8) {
         float v[8];
+        if (edge) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int c = c8 * 8 + e;
-          const int j = bj * BLK + c;
-          const bool vis = row_ok && (j < tile.L) && (!p.causal || j <= row_local);
-          v[e] = vis ? ex2(fmaf(s[c], sc, -m2)) * invl : 0.f;
+          for (int e = 0; e < 8; ++e) {
+            const int c = c8 * 8 + e;
+            const int j = bj * BLK + c;
+            const bool vis = row_ok && (j < tile.L) && (!p.causal || j <= row_local);
+            v[e] = vis ? ex2(fmaf(s[c], sc, -m2)) * invl : 0.f;
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) v[e] = ex2(fmaf(s[c8 * 8 + e], sc, -m2)) * invl;
         }
         uint4 w;
         w.x = pack_bf16x2(v[0], v[1]);
         w.y = pack_bf16x2(v[2], v[3]);
         w.z = pack_bf16x2(v[4], v[5]);
         w.w = pack_bf16x2(v[6], v[7]);
+        constexpr int kBuf = Lay::kStageBytes / 2;
         uint32_t off;
-        if (BLK == 64) off = sub * 8192 + sw128_off(rloc, c8);
-        else off = (c8 >> 3) * 16384 + sw128_off(row, c8 & 7);
+        if (BLK == 64) off = sbuf * kBuf + sub * 8192 + sw128_off(rloc, c8);
+        else off = sbuf * kBuf + (c8 >> 3) * 16384 + sw128_off(row, c8 & 7);
         *reinterpret_cast<uint4*>(stg_g + off) = w;
       }
       fence_async_smem();
       named_bar(bar_id, grp_threads);
       if (leader) {
+        constexpr int kBuf = Lay::kStageBytes / 2;
         const int tidx = ((sub == 0) ? base[0] : base[1]) + pos;
         if (BLK == 64) {
-          tma_store_2d(&tvals, stg + sub * 8192, 0, tidx * 64);
+          tma_store_2d(&tvals, stg + sbuf * kBuf + sub * 8192, 0, tidx * 64);
         } else {
-          tma_store_2d(&tvals, stg, 0, tidx * 128);
-          tma_store_2d(&tvals, stg + 16384, 64, tidx * 128);
+          tma_store_2d(&tvals, stg + sbuf * kBuf, 0, tidx * 128);
+          tma_store_2d(&tvals, stg + sbuf * kBuf + 16384, 64, tidx * 128);
         }
         bulk_commit();
       }

@@ -11,7 +11,9 @@
 // Design", item 3): A_hat_i = sum_h W[i,h] * A_h; a block a head did not keep
 // counts as zero and nothing is renormalised.
 //
-// CTA = (64 query rows of one block-row, one receiver KV group g).  It walks
+// CTA = (64 query rows of one block-row, one receiver KV group g); the group
+// CTAs of a block-row are adjacent in the grid so its tiles are read from HBM
+// about once and served to the other groups from L2.  It walks
 // the ascending union (over sender heads) of the kept block columns of its
 // block-row, in 64-column sub-blocks.  For each sub-block:
 //   warp 0   TMA: V_g rows of the sub-block (64 x d) and, in chunks of four
@@ -78,8 +80,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int hpg = p.H_r / p.H_kv;
   const RetLayout lay(D, hpg);
-  const RowSlab slab = p.slabs[blockIdx.x];
-  const int g = blockIdx.y;
+  // grid x = KV group (fastest), y = slab: the group CTAs of one block-row run
+  // side by side and share its sender tiles through L2
+  const RowSlab slab = p.slabs[blockIdx.y];
+  const int g = blockIdx.x;
   const RowBlock rbk = p.rbs[slab.rb];
   constexpr int kSubPerBlock = BLK / 64;
   const int n_sub = p.union_cnt[slab.rb] * kSubPerBlock;
@@ -354,7 +358,7 @@ cudaError_t launch_ret_t(const RetrieveParams& p, const CUtensorMap& tp, const C
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, lay.bytes);
   if (e != cudaSuccess) return e;
-  dim3 grid(p.n_slabs, p.H_kv);
+  dim3 grid(p.H_kv, p.n_slabs);
   kern<<<grid, kThreads, lay.bytes, s>>>(tp, tv, p, static_cast<__nv_bfloat16*>(o));
   return cudaGetLastError();
 }

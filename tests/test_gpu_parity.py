@@ -60,6 +60,13 @@ def small_case(seqlens, Hs, Hks, d, B, p, Hr, Hkv, dtype="bf16", causal=True, se
     ((300, 129), 3, 3, 128, 128, 8, 2),       # B = 128, ragged
     ((333,), 2, 1, 64, 64, 4, 4),             # d = 64, hpg 1
     ((257, 64), 2, 2, 64, 128, 16, 2),        # d = 64, B = 128, hpg 8
+    # 8 receiver KV heads: the cluster retrieval
+    ((512,), 8, 8, 128, 64, 32, 8),           # 4 heads per group
+    ((200, 137, 64, 1, 130), 8, 4, 128, 64, 24, 8),  # varlen, ragged, GQA sender, 3 per group
+    ((300, 129), 6, 6, 128, 128, 16, 8),      # B = 128, 2 per group
+    ((333,), 3, 3, 64, 64, 8, 8),             # d = 64, 1 per group
+    ((257, 64), 20, 20, 64, 128, 32, 8),      # d = 64, B = 128, padded sender heads
+    ((256,), 64, 64, 128, 64, 32, 8),         # 64 sender heads (one V stage)
 ])
 def test_small_bf16(seqlens, Hs, Hks, d, B, Hr, Hkv):
     small_case(seqlens, Hs, Hks, d, B, 0.95, Hr, Hkv)
@@ -67,6 +74,7 @@ def test_small_bf16(seqlens, Hs, Hks, d, B, Hr, Hkv):
 
 def test_noncausal():
     small_case((190, 70), 2, 2, 128, 64, 0.9, 4, 2, causal=False, structured=False)
+    small_case((190, 70), 4, 4, 128, 64, 0.9, 16, 8, causal=False, structured=False)
 
 
 def test_p1_keeps_every_block_with_mass():
