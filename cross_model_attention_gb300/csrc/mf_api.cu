@@ -261,6 +261,12 @@ int mf_bsr_create(mf_bsr_t* out, int n_layers, int T, int H_s, int B, int causal
                      const int wa = causal ? a.tl : 0, wb = causal ? b.tl : 0;
                      return wa > wb;
                    });
+  // heaviest slabs first (causal: work grows with the block-row index) so the
+  // tail of the retrieval grid is short
+  std::stable_sort(h->slabs.begin(), h->slabs.end(), [&](const RowSlab& a, const RowSlab& b) {
+    const int wa = causal ? h->rbs[a.rb].bi : 0, wb = causal ? h->rbs[b.rb].bi : 0;
+    return wa > wb;
+  });
   h->R = (int)h->rbs.size();
   h->C = (int)cand;
   h->n_tiles = (int)h->tiles.size();
@@ -502,6 +508,7 @@ int mf_retrieve(mf_bsr_t h, const float* W, const void* v, void* o, int dtype, i
     rp.union_list = L.union_list;
     rp.W = W + (size_t)x * H_r * h->H_s;
     rp.zero_tile = (int)L.nnz;
+    rp.values = L.values;
     rp.err = h->err_d;
     const char* vx = static_cast<const char*>(v) + x * v_layer;
     char* ox = static_cast<char*>(o) + x * o_layer;

@@ -64,6 +64,7 @@ struct RetrieveParams {
   const int* union_list;  // [C]
   const float* W;         // [H_r][H_s] of this receiver layer
   int zero_tile;          // index of an all-zero tile (= nnz)
+  const uint16_t* values; // [nnz+1][B][B] bf16 tiles
   int* err;
 };
 

@@ -228,6 +228,15 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t raddr, uint4 v) {
                "r"(v.z), "r"(v.w)
                : "memory");
 }
+// Asynchronous 16-byte store into another CTA's shared memory; on completion
+// it counts 16 transaction bytes on that CTA's mbarrier `rbar`.
+__device__ __forceinline__ void st_async_v4(uint32_t raddr, uint4 v, uint32_t rbar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1,%2,%3,%4}, [%5];" ::"r"(
+          raddr),
+      "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(rbar)
+      : "memory");
+}
 // Arrive on an mbarrier of another CTA of the cluster, releasing this
 // thread's earlier writes at cluster scope.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t raddr) {
@@ -280,6 +289,17 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map
       " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
       "l"(map), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar)
       : "memory");
+}
+// 16-byte asynchronous global->shared copy (L2 only); src_bytes = 0 writes
+// zeros without reading global memory.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+// Arrive on `bar` once this thread's earlier cp.async copies have landed (the
+// barrier's expected count includes this arrival).
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t r;
