@@ -83,7 +83,10 @@ struct LayerState {
   int dtype = -1;
   int d = 0;
   float p = 0.f;
-  long long nnz = 0;
+  long long nnz = 0;       // valid when nnz_known
+  bool nnz_known = false;
+  long long capacity = 0;  // tiles allocated for kept blocks (zero tile at this index)
+  cudaStream_t stream = nullptr;
   void* meta = nullptr;    // one allocation carved into the arrays below
   size_t meta_bytes = 0;
   float* mass = nullptr;
@@ -109,6 +112,7 @@ struct ProfRec {
 };
 
 struct mf_bsr_s {
+  bool exact_alloc = false;  // size the BSR exactly (one stream sync per layer)
   bool profiling = false;
   long long launches[MF_K_COUNT] = {0};
   std::vector<ProfRec> prof;
@@ -410,21 +414,33 @@ int mf_compress(mf_bsr_t h, int layer, const void* q, const void* k, int dtype, 
   }
   MF_CUDA(timed(h, MF_K_SELECT, s, [&] { return launch_select(cp, s); }), "selection kernel");
   MF_CUDA(timed(h, MF_K_SCAN, s, [&] { return launch_scan(cp, s); }), "row_ptr scan kernel");
-  MF_CUDA(cudaMemcpyAsync(&h->host_pinned[0], L.nnz_dev, sizeof(long long), cudaMemcpyDeviceToHost, s),
-          "nnz copy");
-  MF_CUDA(cudaMemcpyAsync(&h->host_pinned[1], h->err_d, sizeof(int), cudaMemcpyDeviceToHost, s),
-          "error word copy");
-  MF_CUDA(cudaStreamSynchronize(s), "compress sync");
-  const int dev_err = static_cast<int>(h->host_pinned[1] & 0xffffffff);
-  if (dev_err) {
-    cudaMemsetAsync(h->err_d, 0, sizeof(int), s);
-    release_layer(h, L, s);
-    return fail(MF_ERR_TIMEOUT, "a device-side wait timed out in the compressor");
+  long long cap;
+  if (h->exact_alloc) {
+    // exact size: learn nnz first (the one host round trip of this mode)
+    MF_CUDA(cudaMemcpyAsync(&h->host_pinned[0], L.nnz_dev, sizeof(long long), cudaMemcpyDeviceToHost, s),
+            "nnz copy");
+    MF_CUDA(cudaMemcpyAsync(&h->host_pinned[1], h->err_d, sizeof(int), cudaMemcpyDeviceToHost, s),
+            "error word copy");
+    MF_CUDA(cudaStreamSynchronize(s), "compress sync");
+    const int dev_err = static_cast<int>(h->host_pinned[1] & 0xffffffff);
+    if (dev_err) {
+      cudaMemsetAsync(h->err_d, 0, sizeof(int), s);
+      release_layer(h, L, s);
+      return fail(MF_ERR_TIMEOUT, "a device-side wait timed out in the compressor");
+    }
+    cap = h->host_pinned[0];
+    L.nnz = cap;
+    L.nnz_known = true;
+  } else {
+    // upper bound (every candidate kept): no host round trip; nnz stays on
+    // the device until someone asks for it
+    cap = (long long)HC;
+    L.nnz_known = false;
   }
-  const long long nnz = h->host_pinned[0];
-  L.nnz = nnz;
-  L.values_bytes = (size_t)nnz * B * B * 2;
-  L.colidx_bytes = (size_t)nnz * 4;
+  L.capacity = cap;
+  L.stream = s;
+  L.values_bytes = (size_t)cap * B * B * 2;
+  L.colidx_bytes = (size_t)cap * 4;
   // one extra all-zero tile after the kept ones: the retrieval reads it in
   // place of a head's dropped block
   L.values = (uint16_t*)dev_alloc(h, L.values_bytes + (size_t)B * B * 2, s);
@@ -437,25 +453,24 @@ int mf_compress(mf_bsr_t h, int layer, const void* q, const void* k, int dtype, 
   MF_CUDA(cudaMemsetAsync(L.tile_of, 0xFF, HC * 4, s), "tile index reset");
   MF_CUDA(cudaMemsetAsync(reinterpret_cast<char*>(L.values) + L.values_bytes, 0, (size_t)B * B * 2, s),
           "zero tile");
-  if (dtype == MF_DTYPE_BF16) {
-    CUtensorMap tvals{};
-    if (nnz > 0) {
-      if ((rc = make_map(&tvals, L.values, B, (uint64_t)nnz * B, (uint64_t)B * 2, 64,
+  if (cap > 0) {
+    if (dtype == MF_DTYPE_BF16) {
+      CUtensorMap tvals{};
+      if ((rc = make_map(&tvals, L.values, B, (uint64_t)cap * B, (uint64_t)B * 2, 64,
                          B == 64 ? 64 : 128)) != MF_OK)
         return rc;
       MF_CUDA(timed(h, MF_K_PACK, s, [&] { return launch_pack_bf16(cp, tq, tk_pack, tvals, s); }),
               "pack kernel");
-    }
-  } else {
-    if (nnz > 0)
+    } else {
       MF_CUDA(timed(h, MF_K_PACK, s,
                     [&] { return launch_pack_f32(cp, (const float*)q, (const float*)k, L.values, s); }),
               "pack kernel (fp32)");
+    }
   }
   MF_CUDA(timed(h, MF_K_UNION, s, [&] { return launch_union(cp, s); }), "union kernel");
-  if ((rc = make_map(&L.pmap, L.values, B, (uint64_t)(nnz + 1) * B, (uint64_t)B * 2, 64, 64)) != MF_OK)
+  if ((rc = make_map(&L.pmap, L.values, B, (uint64_t)(cap + 1) * B, (uint64_t)B * 2, 64, 64)) != MF_OK)
     return rc;
-  if ((rc = make_map(&L.gmap, L.values, B, (uint64_t)(nnz + 1) * B, (uint64_t)B * 2, 64, 1)) != MF_OK)
+  if ((rc = make_map(&L.gmap, L.values, B, (uint64_t)(cap + 1) * B, (uint64_t)B * 2, 64, 1)) != MF_OK)
     return rc;
   L.valid = true;
   L.dtype = dtype;
@@ -507,7 +522,7 @@ int mf_retrieve(mf_bsr_t h, const float* W, const void* v, void* o, int dtype, i
     rp.union_cnt = L.union_cnt;
     rp.union_list = L.union_list;
     rp.W = W + (size_t)x * H_r * h->H_s;
-    rp.zero_tile = (int)L.nnz;
+    rp.zero_tile = (int)L.capacity;
     rp.values = L.values;
     rp.err = h->err_d;
     const char* vx = static_cast<const char*>(v) + x * v_layer;
@@ -536,11 +551,39 @@ int mf_retrieve(mf_bsr_t h, const float* W, const void* v, void* o, int dtype, i
   return MF_OK;
 }
 
+}  // extern "C"
+
+namespace {
+// Reads a layer's kept-tile count from the device (waits for its compress).
+int ensure_nnz(mf_bsr_t h, LayerState& L) {
+  if (L.nnz_known) return MF_OK;
+  MF_CUDA(cudaMemcpyAsync(&h->host_pinned[0], L.nnz_dev, sizeof(long long), cudaMemcpyDeviceToHost,
+                          L.stream),
+          "nnz copy");
+  MF_CUDA(cudaStreamSynchronize(L.stream), "nnz sync");
+  L.nnz = h->host_pinned[0];
+  L.nnz_known = true;
+  return MF_OK;
+}
+}  // namespace
+
+extern "C" {
+
+int mf_bsr_set_exact(mf_bsr_t h, int exact) {
+  if (!h) return fail(MF_ERR_ARG, "handle is NULL");
+  h->exact_alloc = exact != 0;
+  return MF_OK;
+}
+
 int mf_bsr_info(mf_bsr_t h, int layer, int64_t* nnz, int64_t* n_rows, int64_t* n_cand) {
   if (!h) return fail(MF_ERR_ARG, "handle is NULL");
   if (layer < 0 || layer >= h->n_layers) return fail(MF_ERR_ARG, "layer out of range");
-  const LayerState& L = h->layers[layer];
+  LayerState& L = h->layers[layer];
   if (!L.valid) return fail(MF_ERR_STATE, "layer %d has not been compressed", layer);
+  if (nnz) {
+    const int rc = ensure_nnz(h, L);
+    if (rc != MF_OK) return rc;
+  }
   if (nnz) *nnz = L.nnz;
   if (n_rows) *n_rows = (int64_t)h->H_s * h->R;
   if (n_cand) *n_cand = (int64_t)h->H_s * h->C;
@@ -567,16 +610,20 @@ int mf_bsr_copy(mf_bsr_t h, int layer, int32_t* row_ptr, int32_t* col_idx, uint1
                 float* mass, float* row_max, float* row_sum, void* stream) {
   if (!h) return fail(MF_ERR_ARG, "handle is NULL");
   if (layer < 0 || layer >= h->n_layers) return fail(MF_ERR_ARG, "layer out of range");
-  const LayerState& L = h->layers[layer];
+  LayerState& L = h->layers[layer];
   if (!L.valid) return fail(MF_ERR_STATE, "layer %d has not been compressed", layer);
+  if (col_idx || values) {
+    const int rc = ensure_nnz(h, L);
+    if (rc != MF_OK) return rc;
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t HR = (size_t)h->H_s * h->R, HC = (size_t)h->H_s * h->C, HT = (size_t)h->H_s * h->T;
   auto cp = [&](void* dst, const void* src, size_t bytes) {
     return (dst && bytes) ? cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, s) : cudaSuccess;
   };
   MF_CUDA(cp(row_ptr, L.row_ptr, (HR + 1) * 4), "row_ptr copy");
-  MF_CUDA(cp(col_idx, L.col_idx, L.colidx_bytes), "col_idx copy");
-  MF_CUDA(cp(values, L.values, L.values_bytes), "values copy");
+  MF_CUDA(cp(col_idx, L.col_idx, (size_t)L.nnz * 4), "col_idx copy");
+  MF_CUDA(cp(values, L.values, (size_t)L.nnz * h->B * h->B * 2), "values copy");
   MF_CUDA(cp(mass, L.mass, HC * 4), "mass copy");
   MF_CUDA(cp(row_max, L.row_max, HT * 4), "row_max copy");
   MF_CUDA(cp(row_sum, L.row_sum, HT * 4), "row_sum copy");

@@ -15,12 +15,14 @@
 //   warp 0  TMA producer: Q tile once, K tiles (128 keys) into a 3-4 stage ring
 //   warp 1  tcgen05 issuer: S = Q.K^T (M=128, N=128, K=d) into one of two TMEM
 //           buffers (fp32, 128 lanes x 128 columns each)
-//   warps 2-5  statistics, one thread per query row (its TMEM lane):
-//           block max, lazily re-referenced exp2, per-(row, key-block) partial
-//           sums written to TMEM columns 256..511 (so at most 256 key blocks per
-//           row), running row sum.  A row's reference value only moves when the
-//           block max exceeds it by more than 2^8; the stored partials of the
-//           warp are then rescaled in TMEM.
+//   statistics warps, one thread per query row (its TMEM lane): block max,
+//           lazily re-referenced exp2, per-(row, key-block) partial sums kept
+//           in TMEM columns 256..511 (so at most 256 key blocks per row),
+//           running row sum.  A reference value only moves when the block max
+//           exceeds it by more than 2^8; the warp's stored partials are then
+//           rescaled in TMEM.  At B = 64 two warps share each lane quadrant,
+//           one per 64-column block of the S tile, with separate references
+//           that are merged per row at the end (columns 256..383 / 384..511).
 //   end:    mass[bi][bj] = sum over the block-row's rows of partial/l_ref,
 //           reduced across lanes with a 31-shuffle transpose-reduction and
 //           across warps in a fixed order (deterministic).
@@ -46,7 +48,8 @@ struct StatsLayout {
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + kTileBytes;
   static constexpr int kRed = kK + kStages * kTileBytes;    // float [4][256]
-  static constexpr int kBar = kRed + 4 * 256 * 4;           // 16 mbarriers
+  static constexpr int kX = kRed + 4 * 256 * 4;             // float [2][3][128] row-state exchange
+  static constexpr int kBar = kX + 2 * 3 * 128 * 4;         // 16 mbarriers
   static constexpr int kSlot = kBar + 16 * 8;
   static constexpr int kFlag = kSlot + 8;
   static constexpr int kBytes = kFlag + 8 + 1024;           // + alignment slack
@@ -103,8 +106,16 @@ __device__ __forceinline__ void rescale_parts(uint32_t taddr, int ncols, float a
   tc_wait_st();
 }
 
+// Statistics warps: at B = 64 two per TMEM lane quadrant (each owns one
+// 64-column block of every 128-column S tile); at B = 128 one per quadrant.
+template <int BLK>
+struct StatWarps {
+  static constexpr int kN = (BLK == 64) ? 8 : 4;
+  static constexpr int kThreads = 64 + 32 * kN;
+};
+
 template <int D, int BLK>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(StatWarps<BLK>::kThreads, 1)
     stats_bf16_kernel(const __grid_constant__ CUtensorMap tq,
                       const __grid_constant__ CUtensorMap tk, const CompressParams p) {
   using Lay = StatsLayout<D>;
@@ -135,7 +146,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(barSFull(b), 1);
-      mbar_init(barSEmpty(b), 4);
+      mbar_init(barSEmpty(b), StatWarps<BLK>::kN);
     }
     mbar_init(barDone, 1);
     *abort_flag = 0;
@@ -205,11 +216,15 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else {
     // ---------------------------------------------------------- statistics
+    constexpr int kSW = StatWarps<BLK>::kN;
+    constexpr int kW = (BLK == 64) ? 64 : 128;  // S columns per warp per tile (one block)
     const int wq = warp & 3;
+    const int half = (BLK == 64) ? ((warp - 2) >> 2) : 0;
     const int row = wq * 32 + lane;
     const int row_local = tile.tl * kRows + row;
     const bool row_ok = row_local < tile.L;
     const uint32_t trow = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+    const uint32_t partcol = kPartCol + half * 128;  // this warp's per-block partials
     const float sc = p.scale_log2;
     float mtrue = -INFINITY, ref = -INFINITY, lsum = 0.f;
     int nblk = 0;
@@ -221,103 +236,122 @@ __global__ void __launch_bounds__(192, 1)
         break;
       }
       tc_fence_after();
-      float s[kCols];
+      float x[kW];
       {
-        uint32_t* r = reinterpret_cast<uint32_t*>(s);
+        uint32_t* r = reinterpret_cast<uint32_t*>(x);
 #pragma unroll
-        for (int c = 0; c < kCols; c += 32) tmem_ld32(trow + b * kCols + c, r + c);
+        for (int c = 0; c < kW; c += 32) tmem_ld32(trow + b * kCols + half * 64 + c, r + c);
       }
       tc_wait_ld();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(barSEmpty(b));
-      const bool last = (n == n_ct - 1);
+      const int col0 = n * kCols + half * 64;
+      float bm = -INFINITY;
+      if (n == n_ct - 1) {  // only the last tile can cross the diagonal or the sequence end
 #pragma unroll
-      for (int hb = 0; hb < kCols / BLK; ++hb) {
-        float* x = s + hb * BLK;
-        const int col0 = n * kCols + hb * BLK;
-        float bm = -INFINITY;
-        if (last) {
+        for (int c = 0; c < kW; ++c) {
+          const int j = col0 + c;
+          const bool vis = (j < tile.L) && (!p.causal || j <= row_local);
+          x[c] = vis ? x[c] * sc : -INFINITY;
+          bm = fmaxf(bm, x[c]);
+        }
+      } else {
 #pragma unroll
-          for (int c = 0; c < BLK; ++c) {
-            const int j = col0 + c;
-            const bool vis = (j < tile.L) && (!p.causal || j <= row_local);
-            x[c] = vis ? x[c] * sc : -INFINITY;
-            bm = fmaxf(bm, x[c]);
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < BLK; ++c) {
-            x[c] *= sc;
-            bm = fmaxf(bm, x[c]);
-          }
+        for (int c = 0; c < kW; ++c) {
+          x[c] *= sc;
+          bm = fmaxf(bm, x[c]);
         }
-        if (!row_ok) bm = -INFINITY;
-        mtrue = fmaxf(mtrue, bm);
-        float alpha = 1.f;
-        if (bm > ref + kTau) {
-          alpha = (ref == -INFINITY) ? 0.f : ex2(ref - bm);
-          ref = bm;
-          lsum *= alpha;
-        }
-        if (__any_sync(0xffffffffu, alpha != 1.f) && nblk > 0) {
-          tc_wait_st();
-          rescale_parts(trow + kPartCol, nblk, alpha);
-        }
-        const float rs = (ref == -INFINITY) ? 0.f : ref;
-        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-        for (int c = 0; c < BLK; c += 4) {
-          a0 += ex2(x[c] - rs);
-          a1 += ex2(x[c + 1] - rs);
-          a2 += ex2(x[c + 2] - rs);
-          a3 += ex2(x[c + 3] - rs);
-        }
-        float bs = (a0 + a1) + (a2 + a3);
-        if (!row_ok) bs = 0.f;
-        lsum += bs;
-        tmem_st1(trow + kPartCol + nblk, __float_as_uint(bs));
-        ++nblk;
       }
+      if (!row_ok) bm = -INFINITY;
+      mtrue = fmaxf(mtrue, bm);
+      float alpha = 1.f;
+      if (bm > ref + kTau) {
+        alpha = (ref == -INFINITY) ? 0.f : ex2(ref - bm);
+        ref = bm;
+        lsum *= alpha;
+      }
+      if (__any_sync(0xffffffffu, alpha != 1.f) && nblk > 0) {
+        tc_wait_st();
+        rescale_parts(trow + partcol, nblk, alpha);
+      }
+      const float rs = (ref == -INFINITY) ? 0.f : ref;
+      float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+      for (int c = 0; c < kW; c += 4) {
+        a0 += ex2(x[c] - rs);
+        a1 += ex2(x[c + 1] - rs);
+        a2 += ex2(x[c + 2] - rs);
+        a3 += ex2(x[c + 3] - rs);
+      }
+      float bs = (a0 + a1) + (a2 + a3);
+      if (!row_ok) bs = 0.f;
+      lsum += bs;
+      tmem_st1(trow + partcol + nblk, __float_as_uint(bs));
+      ++nblk;
     }
     tc_wait_st();
     // -------------------------------------------------------- epilogue
     const bool good = ok && (*abort_flag == 0);
-    const float inv = (row_ok && lsum > 0.f) ? 1.f / lsum : 0.f;
-    if (good && row_ok) {
+    float M = mtrue, Rf = ref, Lt = lsum, own_scale = 1.f;
+    if (BLK == 64) {
+      // merge the two column halves of each row (separate lazy references)
+      float* xs = reinterpret_cast<float*>(smem + Lay::kX);
+      xs[(half * 3 + 0) * 128 + row] = mtrue;
+      xs[(half * 3 + 1) * 128 + row] = ref;
+      xs[(half * 3 + 2) * 128 + row] = lsum;
+      named_bar(1, 32 * kSW);
+      const int oh = half ^ 1;
+      const float mo = xs[(oh * 3 + 0) * 128 + row], ro = xs[(oh * 3 + 1) * 128 + row],
+                  lo = xs[(oh * 3 + 2) * 128 + row];
+      M = fmaxf(mtrue, mo);
+      Rf = fmaxf(ref, ro);
+      if (Rf == -INFINITY) {
+        Lt = 0.f;
+      } else {
+        own_scale = (ref == -INFINITY) ? 0.f : ex2(ref - Rf);
+        const float other = (ro == -INFINITY) ? 0.f : ex2(ro - Rf);
+        Lt = lsum * own_scale + lo * other;
+      }
+    }
+    const float inv = (row_ok && Lt > 0.f) ? own_scale / Lt : 0.f;
+    if (good && row_ok && half == 0) {
       const size_t o = static_cast<size_t>(h) * p.T + tile.seq_start + row_local;
-      p.row_max[o] = mtrue * kLn2;
-      p.row_sum[o] = lsum * ex2(ref - mtrue);
+      p.row_max[o] = M * kLn2;
+      p.row_sum[o] = Lt * ex2(Rf - M);
     }
     float* red = reinterpret_cast<float*>(smem + Lay::kRed);
     for (int c0 = 0; c0 < nblk; c0 += 32) {
       uint32_t v[32];
-      tmem_ld32(trow + kPartCol + c0, v);
+      tmem_ld32(trow + partcol + c0, v);
       tc_wait_ld();
       float f[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) f[i] = (c0 + i < nblk) ? __uint_as_float(v[i]) * inv : 0.f;
-      red[wq * 256 + c0 + lane] = transpose_reduce32(f);
+      const float tot = transpose_reduce32(f);
+      const int k = c0 + lane;
+      if (k < nblk) red[wq * 256 + (BLK == 64 ? 2 * k + half : k)] = tot;
     }
     tc_fence_before();
-    named_bar(1, 128);
+    named_bar(1, 32 * kSW);
     if (good) {
       const int t0 = threadIdx.x - 64;
+      const int nbt = (BLK == 64) ? 2 * nblk : nblk;  // block columns covered
       if (BLK == 64) {
-        for (int t = t0; t < 2 * nblk; t += 128) {
-          const int half = t / nblk, c = t - half * nblk;
-          const int bi = tile.tl * 2 + half;
+        for (int t = t0; t < 2 * nbt; t += 32 * kSW) {
+          const int hb = t / nbt, c = t - hb * nbt;
+          const int bi = tile.tl * 2 + hb;
           if (bi * 64 >= tile.L) continue;
-          const RowBlock rbk = p.rbs[tile.rb0 + half];
+          const RowBlock rbk = p.rbs[tile.rb0 + hb];
           const int ncand = p.causal ? rbk.bi + 1 : (tile.L + 63) / 64;
           if (c >= ncand) continue;
-          const float m = red[(2 * half) * 256 + c] + red[(2 * half + 1) * 256 + c];
+          const float m = red[(2 * hb) * 256 + c] + red[(2 * hb + 1) * 256 + c];
           p.mass[static_cast<size_t>(h) * p.C + rbk.cand_off + c] = m;
         }
       } else {
         const RowBlock rbk = p.rbs[tile.rb0];
         const int ncand = p.causal ? rbk.bi + 1 : (tile.L + BLK - 1) / BLK;
-        for (int c = t0; c < ncand; c += 128) {
+        for (int c = t0; c < ncand; c += 32 * kSW) {
           const float m = (red[c] + red[256 + c]) + (red[512 + c] + red[768 + c]);
           p.mass[static_cast<size_t>(h) * p.C + rbk.cand_off + c] = m;
         }
@@ -341,7 +375,7 @@ cudaError_t launch_stats_t(const CompressParams& p, const CUtensorMap& tq, const
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(p.n_tiles, p.H_s);
-  kern<<<grid, 192, smem, s>>>(tq, tk, p);
+  kern<<<grid, StatWarps<BLK>::kThreads, smem, s>>>(tq, tk, p);
   return cudaGetLastError();
 }
 

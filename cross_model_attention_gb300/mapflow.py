@@ -22,7 +22,7 @@ MF_DTYPE_F32, MF_DTYPE_BF16 = 0, 1
 EXPORTED = ("mf_version", "mf_last_error", "mf_supported", "mf_bsr_create", "mf_bsr_destroy",
             "mf_compress", "mf_retrieve", "mf_bsr_info", "mf_bsr_export", "mf_bsr_copy",
             "mf_bsr_release_layer", "mf_device_status", "mf_selftest_wait", "mf_profile",
-            "mf_profile_read", "mf_select_noalloc")
+            "mf_profile_read", "mf_select_noalloc", "mf_bsr_set_exact")
 KERNELS = ("stats", "select", "scan", "pack", "union", "retrieve")
 
 
@@ -63,6 +63,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mf_bsr_export.argtypes = [vp, i32] + [ctypes.POINTER(vp)] * 6
     lib.mf_bsr_copy.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp, vp]
     lib.mf_bsr_release_layer.argtypes = [vp, i32]
+    lib.mf_bsr_set_exact.argtypes = [vp, i32]
     lib.mf_device_status.argtypes = [vp, vp]
     lib.mf_selftest_wait.argtypes = [vp, i32, vp]
     lib.mf_select_noalloc.argtypes = [vp, ctypes.POINTER(ctypes.c_int32), i32, i32, i32, i32,
@@ -161,6 +162,10 @@ def mf_retrieve(h, W, v, o, H_r: int, H_kv: int, d: int, layer_map: Sequence[int
                                        _stream(stream)))
 
 
+def mf_bsr_set_exact(h, exact: bool) -> None:
+    _check(load_library().mf_bsr_set_exact(h, int(exact)))
+
+
 def mf_bsr_info(h, layer: int):
     a, b, c = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
     _check(load_library().mf_bsr_info(h, layer, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)))
@@ -227,6 +232,9 @@ class BSR:
         n, T, H_kv, d = v.shape
         H_r = o.shape[2]
         mf_retrieve(self.handle, W, v, o, H_r, H_kv, d, layer_map, stream)
+
+    def set_exact(self, exact: bool) -> None:
+        mf_bsr_set_exact(self.handle, exact)
 
     def info(self, layer: int):
         return mf_bsr_info(self.handle, layer)

@@ -142,9 +142,14 @@ MF_API void mf_bsr_destroy(mf_bsr_t h);
  *                               block, ascending within a row
  *   values  bf16  [nnz][B][B]   P_ij = exp(s_ij - m_i)/l_i, zero above the
  *                               diagonal and outside the sequence
- * It synchronises `stream` once (to size the values buffer from nnz).
+ * By default the call is fully asynchronous: the values buffer is sized for
+ * the upper bound (every candidate kept, plus one all-zero tile used by the
+ * retrieval) and nnz stays on the device until mf_bsr_info/_copy asks for it;
+ * a device-side timeout is then reported by mf_device_status.  After
+ * mf_bsr_set_exact(h, 1) the call instead synchronises `stream` once to size
+ * the buffer exactly and reports MF_ERR_TIMEOUT itself.
  * Errors: MF_ERR_ARG, MF_ERR_UNSUPPORTED, MF_ERR_OOM, MF_ERR_CUDA,
- * MF_ERR_TIMEOUT (a device wait gave up; the layer is left empty).
+ * MF_ERR_TIMEOUT (exact mode: a device wait gave up; the layer is left empty).
  */
 MF_API int mf_compress(mf_bsr_t h, int layer, const void* q, const void* k, int dtype,
                 int T, int H_s, int H_ks, int d, int B, float p, int causal,
@@ -177,8 +182,16 @@ MF_API int mf_retrieve(mf_bsr_t h, const float* W, const void* v, void* o, int d
                 void* stream);
 
 /*
+ * mf_bsr_set_exact — 1: size each layer's BSR exactly (mf_compress then
+ * synchronises its stream once); 0 (default): allocate the upper bound and
+ * never synchronise.
+ */
+MF_API int mf_bsr_set_exact(mf_bsr_t h, int exact);
+
+/*
  * mf_bsr_info — sizes of a compressed layer: nnz (kept tiles), rows
- * (H_s*R), candidates (H_s * sum of candidate blocks per block-row).
+ * (H_s*R), candidates (H_s * sum of candidate blocks per block-row).  Asking
+ * for nnz of an asynchronously compressed layer waits for that compress.
  */
 MF_API int mf_bsr_info(mf_bsr_t h, int layer, int64_t* nnz, int64_t* n_rows, int64_t* n_cand);
 

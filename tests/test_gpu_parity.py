@@ -222,3 +222,29 @@ def test_full_workload3(p):
 
 def test_full_workload4_two_receivers():
     full_size(4)
+
+
+def test_exact_and_bound_allocation_agree():
+    """mf_compress sized exactly (one sync) and at the upper bound (no sync)
+    produce the same BSR and the same retrieval output."""
+    seqlens = (700, 333)
+    T = sum(seqlens)
+    cu = np.concatenate([[0], np.cumsum(seqlens)]).astype(np.int32)
+    w = workloads.scaled(workloads.get(1), seqlens, sender_heads=8, sender_kv_heads=8)
+    x = synth.sender_qk(w, 1)
+    v = synth.random_v(T, 8, 128, 3)["v"][None]
+    W = synth.random_w(32, 8, 4)[None]
+    outs = []
+    for exact in (True, False):
+        bsr = mapflow.BSR(1, T, 8, 64, cu)
+        bsr.set_exact(exact)
+        gc.run_compress(bsr, 0, x, "bf16", 0.9)
+        ex = gc.export_np(bsr, 0)
+        O = gc.run_retrieve(bsr, W, v, 32, "bf16", [0])
+        outs.append((ex, O))
+        bsr.close()
+    (a, Oa), (b, Ob) = outs
+    for key in ("row_ptr", "col_idx", "mass", "row_max", "row_sum"):
+        assert np.array_equal(a[key], b[key]), key
+    assert torch.equal(a["values_dev"].view(torch.int16), b["values_dev"].view(torch.int16))
+    assert np.array_equal(Oa, Ob)
