@@ -11,8 +11,9 @@
 //
 // CTA = (128 query rows = one or two block-rows, one sender head); it walks the
 // ascending union of the kept block columns of its block-rows.  Warp roles as
-// in the statistics kernel: warp 0 TMA loads, warp 1 tcgen05 issue, warps 2-5
-// one thread per query row.  The CTA also writes col_idx and the per-(block,
+// in the statistics kernel: warp 0 TMA loads, warp 1 tcgen05 issue, warps 2-9
+// normalise and store (two per TMEM lane quadrant, one per half of the
+// block's columns).  The CTA also writes col_idx and the per-(block,
 // head) tile index used by the retrieval.
 #include <cmath>
 
@@ -36,8 +37,8 @@ struct PackLayout {
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + kQBytes;
   static constexpr int kStg = kK + kStages * kKBytes;
-  static constexpr int kU = kStg + kStageBytes;        // int [3][kMaxU]
-  static constexpr int kBar = kU + 3 * kMaxU * 4;
+  static constexpr int kU = kStg + kStageBytes;        // int [5][kMaxU]: union + two flag arrays
+  static constexpr int kBar = kU + 5 * kMaxU * 4;
   static constexpr int kSlot = kBar + 16 * 8;
   static constexpr int kMisc = kSlot + 8;
   static constexpr int kBytes = kMisc + 16 + 1024;
@@ -52,8 +53,12 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int* er
   return ok != 0;
 }
 
+// Writer warps: two per TMEM lane quadrant, each normalising half of the
+// block's columns.
+constexpr int kPackThreads = 64 + 256;
+
 template <int D, int BLK>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kPackThreads, (BLK == 64) ? 2 : 1)
     pack_bf16_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                      const __grid_constant__ CUtensorMap tvals, const CompressParams p) {
   using Lay = PackLayout<D, BLK>;
@@ -70,6 +75,8 @@ __global__ void __launch_bounds__(192, 1)
   int* u_bj = reinterpret_cast<int*>(smem + Lay::kU);
   int* u_pos0 = u_bj + kMaxU;
   int* u_pos1 = u_pos0 + kMaxU;
+  int* fl0 = u_pos1 + kMaxU;  // position of column bj in kept list 0 (or -1)
+  int* fl1 = fl0 + kMaxU;
   volatile int* misc = reinterpret_cast<volatile int*>(smem + Lay::kMisc);  // [0]=n_u [1]=abort
 
   const uint32_t barQ = sb + Lay::kBar;
@@ -107,35 +114,49 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(barSFull(b), 1);
-      mbar_init(barSEmpty(b), 4);
+      mbar_init(barSEmpty(b), 8);
     }
     mbar_init(barDone, 1);
     fence_mbar_init();
-    // ascending union of the kept lists with each list's position
-    int i0 = 0, i1 = 0, n = 0;
-    while ((i0 < kc[0] || i1 < kc[1]) && n < kMaxU) {
-      const int a = i0 < kc[0] ? kl[0][i0] : 0x7fffffff;
-      const int b = i1 < kc[1] ? kl[1][i1] : 0x7fffffff;
-      const int bj = a < b ? a : b;
-      u_bj[n] = bj;
-      u_pos0[n] = (a == bj) ? i0++ : -1;
-      u_pos1[n] = (b == bj) ? i1++ : -1;
-      ++n;
-    }
-    misc[0] = n;
     misc[1] = 0;
   }
-  // col_idx and the retrieval's tile index of every kept (block, head)
-  if (threadIdx.x >= 64) {
-    for (int t = 0; t < 2; ++t) {
-      if (rbv[t] < 0) continue;
-      const RowBlock rbk = p.rbs[rbv[t]];
-      for (int i = threadIdx.x - 64; i < kc[t]; i += 128) {
-        const int bj = kl[t][i];
-        p.col_idx[base[t] + i] = bj;
-        p.tile_of[static_cast<size_t>(rbk.cand_off + bj) * p.H_s + h] = base[t] + i;
-      }
+  // ascending union of the two kept lists, in parallel: mark each list's
+  // columns, then compact with warp ballots
+  const int nbj = p.causal ? (tile.tl + 1) * (kRows / BLK) : (tile.L + BLK - 1) / BLK;
+  for (int i = threadIdx.x; i < kMaxU; i += blockDim.x) {
+    fl0[i] = -1;
+    fl1[i] = -1;
+  }
+  __syncthreads();
+  for (int t = 0; t < 2; ++t) {
+    if (rbv[t] < 0) continue;
+    const RowBlock rbk = p.rbs[rbv[t]];
+    int* fl = t ? fl1 : fl0;
+    for (int i = threadIdx.x; i < kc[t]; i += blockDim.x) {
+      const int bj = kl[t][i];
+      fl[bj] = i;
+      // col_idx and the retrieval's tile index of every kept (block, head)
+      p.col_idx[base[t] + i] = bj;
+      p.tile_of[static_cast<size_t>(rbk.cand_off + bj) * p.H_s + h] = base[t] + i;
     }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int n = 0;
+    for (int c0 = 0; c0 < nbj; c0 += 32) {
+      const int bj = c0 + lane;
+      const int a = (bj < nbj) ? fl0[bj] : -1, b = (bj < nbj) ? fl1[bj] : -1;
+      const bool f = (a >= 0) || (b >= 0);
+      const uint32_t m = __ballot_sync(0xffffffffu, f);
+      if (f) {
+        const int pos = n + __popc(m & ((1u << lane) - 1u));
+        u_bj[pos] = bj;
+        u_pos0[pos] = a;
+        u_pos1[pos] = b;
+      }
+      n += __popc(m);
+    }
+    if (lane == 0) misc[0] = n;
   }
   if (warp == 1) tmem_alloc(sb + Lay::kSlot, 2 * kN < 32 ? 32 : 2 * kN);
   tc_fence_before();
@@ -202,7 +223,9 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else {
     // ------------------------------------------------ normalise + store
+    constexpr int kHalfCols = BLK / 2;  // columns per writer warp
     const int wq = warp & 3;
+    const int ch = (warp - 2) >> 2;     // column half of this warp
     const int row = wq * 32 + lane;
     const int row_local = tile.tl * kRows + row;
     const bool row_ok = row_local < tile.L;
@@ -216,23 +239,25 @@ __global__ void __launch_bounds__(192, 1)
       m2 = p.row_max[o] * 1.4426950408889634f;
       invl = 1.f / p.row_sum[o];
     }
-    // staging: BLK=64 -> two 8 KB tiles (one per block-row half);
-    //          BLK=128 -> one 32 KB tile as two 64-column 16 KB boxes
+    // staging: BLK=64 -> per buffer two 8 KB tiles (one per block-row);
+    //          BLK=128 -> per buffer one 32 KB tile as two 64-column boxes
     const uint32_t stg = sb + Lay::kStg;
     uint8_t* stg_g = smem + Lay::kStg;
-    const int grp_threads = (BLK == 64) ? 64 : 128;
+    constexpr int kBuf = Lay::kStageBytes / 2;
+    const int grp_threads = (BLK == 64) ? 128 : 256;
     const int bar_id = (BLK == 64) ? 2 + sub : 2;
-    const bool leader = (BLK == 64) ? (rloc == 0) : (row == 0);
+    const bool leader = ((BLK == 64) ? (rloc == 0) : (row == 0)) && ch == 0;
+    const float2 sc2 = make_float2(sc, sc), nm2 = make_float2(-m2, -m2), il2 = make_float2(invl, invl);
     int nstore = 0;
     for (int u = 0; u < n_u; ++u) {
       const int b = u & 1;
       if (!warp_wait(barSFull(b), (u >> 1) & 1, p.err)) break;
       tc_fence_after();
-      float s[BLK];
+      float s[kHalfCols];
       {
         uint32_t* r = reinterpret_cast<uint32_t*>(s);
 #pragma unroll
-        for (int c = 0; c < BLK; c += 32) tmem_ld32(trow + b * kN + c, r + c);
+        for (int c = 0; c < kHalfCols; c += 32) tmem_ld32(trow + b * kN + ch * kHalfCols + c, r + c);
       }
       tc_wait_ld();
       tc_fence_before();
@@ -250,36 +275,41 @@ __global__ void __launch_bounds__(192, 1)
       // only the diagonal block and the sequence's last block need masking
       const bool edge = !row_ok || (bj * BLK + BLK > tile.L) ||
                         (p.causal && bj * BLK + BLK - 1 > tile.tl * kRows + (row - rloc));
+      const int c_base = ch * kHalfCols;
 #pragma unroll
-      for (int c8 = 0; c8 < BLK / 8; ++c8) {
+      for (int c8 = 0; c8 < kHalfCols / 8; ++c8) {
         float v[8];
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+          float2 t = ffma2(make_float2(s[c8 * 8 + e], s[c8 * 8 + e + 1]), sc2, nm2);
+          t.x = ex2(t.x);
+          t.y = ex2(t.y);
+          t = fmul2(t, il2);
+          v[e] = t.x;
+          v[e + 1] = t.y;
+        }
         if (edge) {
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
-            const int c = c8 * 8 + e;
-            const int j = bj * BLK + c;
+            const int j = bj * BLK + c_base + c8 * 8 + e;
             const bool vis = row_ok && (j < tile.L) && (!p.causal || j <= row_local);
-            v[e] = vis ? ex2(fmaf(s[c], sc, -m2)) * invl : 0.f;
+            if (!vis) v[e] = 0.f;
           }
-        } else {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) v[e] = ex2(fmaf(s[c8 * 8 + e], sc, -m2)) * invl;
         }
         uint4 w;
         w.x = pack_bf16x2(v[0], v[1]);
         w.y = pack_bf16x2(v[2], v[3]);
         w.z = pack_bf16x2(v[4], v[5]);
         w.w = pack_bf16x2(v[6], v[7]);
-        constexpr int kBuf = Lay::kStageBytes / 2;
+        const int cc = (c_base >> 3) + c8;  // 16-byte chunk in the B-column row
         uint32_t off;
-        if (BLK == 64) off = sbuf * kBuf + sub * 8192 + sw128_off(rloc, c8);
-        else off = sbuf * kBuf + (c8 >> 3) * 16384 + sw128_off(row, c8 & 7);
+        if (BLK == 64) off = sbuf * kBuf + sub * 8192 + sw128_off(rloc, cc);
+        else off = sbuf * kBuf + (cc >> 3) * 16384 + sw128_off(row, cc & 7);
         *reinterpret_cast<uint4*>(stg_g + off) = w;
       }
       fence_async_smem();
       named_bar(bar_id, grp_threads);
       if (leader) {
-        constexpr int kBuf = Lay::kStageBytes / 2;
         const int tidx = ((sub == 0) ? base[0] : base[1]) + pos;
         if (BLK == 64) {
           tma_store_2d(&tvals, stg + sbuf * kBuf + sub * 8192, 0, tidx * 64);
@@ -309,7 +339,7 @@ cudaError_t launch_pack_t(const CompressParams& p, const CUtensorMap& tq, const 
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(p.n_tiles, p.H_s);
-  kern<<<grid, 192, smem, s>>>(tq, tk, tv, p);
+  kern<<<grid, kPackThreads, smem, s>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 

@@ -318,6 +318,33 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   asm("max.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
   return y;
 }
+// Packed fp32x2 arithmetic (one issue slot for two lanes of work).
+union F2U64 {
+  float2 f;
+  unsigned long long u;
+};
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  F2U64 A, Bv, C, R;
+  A.f = a;
+  Bv.f = b;
+  C.f = c;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(R.u) : "l"(A.u), "l"(Bv.u), "l"(C.u));
+  return R.f;
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  F2U64 A, Bv, R;
+  A.f = a;
+  Bv.f = b;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(R.u) : "l"(A.u), "l"(Bv.u));
+  return R.f;
+}
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+  F2U64 A, Bv, R;
+  A.f = a;
+  Bv.f = b;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(R.u) : "l"(A.u), "l"(Bv.u));
+  return R.f;
+}
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);

@@ -247,22 +247,21 @@ __global__ void __launch_bounds__(StatWarps<BLK>::kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(barSEmpty(b));
       const int col0 = n * kCols + half * 64;
-      float bm = -INFINITY;
       if (n == n_ct - 1) {  // only the last tile can cross the diagonal or the sequence end
 #pragma unroll
         for (int c = 0; c < kW; ++c) {
           const int j = col0 + c;
-          const bool vis = (j < tile.L) && (!p.causal || j <= row_local);
-          x[c] = vis ? x[c] * sc : -INFINITY;
-          bm = fmaxf(bm, x[c]);
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < kW; ++c) {
-          x[c] *= sc;
-          bm = fmaxf(bm, x[c]);
+          if (!((j < tile.L) && (!p.causal || j <= row_local))) x[c] = -INFINITY;
         }
       }
+      // block max on the raw scores (scaling by sc > 0 preserves order)
+      float m0 = -INFINITY, m1 = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kW; c += 4) {
+        m0 = fmax3(m0, x[c], x[c + 1]);
+        m1 = fmax3(m1, x[c + 2], x[c + 3]);
+      }
+      float bm = fmaxf(m0, m1) * sc;
       if (!row_ok) bm = -INFINITY;
       mtrue = fmaxf(mtrue, bm);
       float alpha = 1.f;
@@ -275,16 +274,22 @@ __global__ void __launch_bounds__(StatWarps<BLK>::kThreads, 1)
         tc_wait_st();
         rescale_parts(trow + partcol, nblk, alpha);
       }
-      const float rs = (ref == -INFINITY) ? 0.f : ref;
-      float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+      // exp2(x * sc - ref) with one packed FMA per two scores, packed sums
+      const float nrs = (ref == -INFINITY) ? 0.f : -ref;
+      const float2 sc2 = make_float2(sc, sc), nrs2 = make_float2(nrs, nrs);
+      float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll
       for (int c = 0; c < kW; c += 4) {
-        a0 += ex2(x[c] - rs);
-        a1 += ex2(x[c + 1] - rs);
-        a2 += ex2(x[c + 2] - rs);
-        a3 += ex2(x[c + 3] - rs);
+        float2 t0 = ffma2(make_float2(x[c], x[c + 1]), sc2, nrs2);
+        float2 t1 = ffma2(make_float2(x[c + 2], x[c + 3]), sc2, nrs2);
+        t0.x = ex2(t0.x);
+        t0.y = ex2(t0.y);
+        t1.x = ex2(t1.x);
+        t1.y = ex2(t1.y);
+        acc0 = fadd2(acc0, t0);
+        acc1 = fadd2(acc1, t1);
       }
-      float bs = (a0 + a1) + (a2 + a3);
+      float bs = (acc0.x + acc0.y) + (acc1.x + acc1.y);
       if (!row_ok) bs = 0.f;
       lsum += bs;
       tmem_st1(trow + partcol + nblk, __float_as_uint(bs));
