@@ -3,6 +3,7 @@
 #pragma once
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <atomic>
 #include <cstdint>
 
 namespace mf {
@@ -67,6 +68,23 @@ struct RetrieveParams {
   const uint16_t* values; // [nnz+1][B][B] bf16 tiles
   int* err;
 };
+
+// SM count of the current device, queried once per device.
+inline cudaError_t sm_count(int* out) {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  int v = cache[dev].load(std::memory_order_relaxed);
+  if (v == 0) {
+    e = cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    cache[dev].store(v, std::memory_order_relaxed);
+  }
+  *out = v;
+  return cudaSuccess;
+}
 
 // -------------------------------------------------------------- launchers --
 // All return cudaError_t of the launch (cudaSuccess when enqueued).

@@ -45,12 +45,12 @@ struct StatsLayout {
   static constexpr int kChunkBytes = kRows * 128;           // 128 rows x 64 bf16
   static constexpr int kTileBytes = kRows * D * 2;
   static constexpr int kStages = (D == 128) ? 3 : 4;
-  static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kTileBytes;
+  static constexpr int kQ = 0;                              // two Q buffers
+  static constexpr int kK = kQ + 2 * kTileBytes;
   static constexpr int kRed = kK + kStages * kTileBytes;    // float [4][256]
   static constexpr int kX = kRed + 4 * 256 * 4;             // float [2][3][128] row-state exchange
-  static constexpr int kBar = kX + 2 * 3 * 128 * 4;         // 16 mbarriers
-  static constexpr int kSlot = kBar + 16 * 8;
+  static constexpr int kBar = kX + 2 * 3 * 128 * 4;         // 24 mbarriers
+  static constexpr int kSlot = kBar + 24 * 8;
   static constexpr int kFlag = kSlot + 8;
   static constexpr int kBytes = kFlag + 8 + 1024;           // + alignment slack
 };
@@ -114,6 +114,17 @@ struct StatWarps {
   static constexpr int kThreads = 64 + 32 * kN;
 };
 
+// Item r of this CTA in a snake order over the heavy-first (tile, head) list:
+// round r takes items [r*G, r*G+G), walked forwards on even rounds and
+// backwards on odd ones, so every CTA's total work stays within one item of
+// the others.  -1 once the list is exhausted.
+__device__ __forceinline__ int item_of(int r, int n_items) {
+  const int G = gridDim.x;
+  const int idx = r * G + ((r & 1) ? (G - 1 - static_cast<int>(blockIdx.x))
+                                    : static_cast<int>(blockIdx.x));
+  return idx < n_items ? idx : -1;
+}
+
 template <int D, int BLK>
 __global__ void __launch_bounds__(StatWarps<BLK>::kThreads, 1)
     stats_bf16_kernel(const __grid_constant__ CUtensorMap tq,
@@ -125,21 +136,22 @@ __global__ void __launch_bounds__(StatWarps<BLK>::kThreads, 1)
                                              ~uintptr_t(1023));
   const uint32_t sb = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const RowTile tile = p.tiles[blockIdx.x];
-  const int h = blockIdx.y;
-  const int hk = h / (p.H_s / p.H_ks);
-  const int n_ct = p.causal ? tile.tl + 1 : (tile.L + kCols - 1) / kCols;
+  const int n_items = p.n_tiles * p.H_s;
 
-  const uint32_t barQ = sb + Lay::kBar;
-  auto barFull = [&](int s) { return sb + Lay::kBar + 8u * (1 + s); };
-  auto barEmpty = [&](int s) { return sb + Lay::kBar + 8u * (1 + NS + s); };
-  auto barSFull = [&](int b) { return sb + Lay::kBar + 8u * (1 + 2 * NS + b); };
-  auto barSEmpty = [&](int b) { return sb + Lay::kBar + 8u * (3 + 2 * NS + b); };
-  const uint32_t barDone = sb + Lay::kBar + 8u * (5 + 2 * NS);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::kFlag);
+  auto barQFull = [&](int q) { return sb + Lay::kBar + 8u * q; };
+  auto barQEmpty = [&](int q) { return sb + Lay::kBar + 8u * (2 + q); };
+  auto barFull = [&](int s) { return sb + Lay::kBar + 8u * (4 + s); };
+  auto barEmpty = [&](int s) { return sb + Lay::kBar + 8u * (4 + NS + s); };
+  auto barSFull = [&](int b) { return sb + Lay::kBar + 8u * (4 + 2 * NS + b); };
+  auto barSEmpty = [&](int b) { return sb + Lay::kBar + 8u * (6 + 2 * NS + b); };
+  const uint32_t barDone = sb + Lay::kBar + 8u * (8 + 2 * NS);
+  volatile int* stat_fail = reinterpret_cast<volatile int*>(smem + Lay::kFlag);
 
   if (threadIdx.x == 0) {
-    mbar_init(barQ, 1);
+    for (int q = 0; q < 2; ++q) {
+      mbar_init(barQFull(q), 1);
+      mbar_init(barQEmpty(q), 1);
+    }
     for (int s = 0; s < NS; ++s) {
       mbar_init(barFull(s), 1);
       mbar_init(barEmpty(s), 1);
@@ -149,7 +161,7 @@ __global__ void __launch_bounds__(StatWarps<BLK>::kThreads, 1)
       mbar_init(barSEmpty(b), StatWarps<BLK>::kN);
     }
     mbar_init(barDone, 1);
-    *abort_flag = 0;
+    *stat_fail = 0;
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(sb + Lay::kSlot, 512);
@@ -160,56 +172,83 @@ __global__ void __launch_bounds__(StatWarps<BLK>::kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // Q of item r into buffer r&1, K tiles of every item through one ring
     if (lane == 0) {
       prefetch_tmap(&tq);
       prefetch_tmap(&tk);
-      const int qrow = tile.seq_start + tile.tl * kRows;
-      mbar_arrive_tx(barQ, Lay::kTileBytes);
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c)
-        tma_load_2d(sb + Lay::kQ + c * Lay::kChunkBytes, &tq, h * D + c * 64, qrow, barQ);
-      int issued = 0;
-      for (int n = 0; n < n_ct; ++n) {
-        const int s = n % NS;
-        if (!mbar_wait(barEmpty(s), ((n / NS) & 1) ^ 1, p.err)) {
-          *abort_flag = 1;
-          break;
-        }
-        mbar_arrive_tx(barFull(s), Lay::kTileBytes);
-        const uint32_t dst = sb + Lay::kK + s * Lay::kTileBytes;
+      int kt = 0, nq = 0;
+      bool ok = true;
+      for (int r = 0; ok; ++r) {
+        const int idx = item_of(r, n_items);
+        if (idx < 0) break;
+        const RowTile tile = p.tiles[idx / p.H_s];
+        const int h = idx % p.H_s;
+        const int hk = h / (p.H_s / p.H_ks);
+        const int n_ct = p.causal ? tile.tl + 1 : (tile.L + kCols - 1) / kCols;
+        const int qb = r & 1;
+        if (!mbar_wait(barQEmpty(qb), ((r >> 1) & 1) ^ 1, p.err)) break;
+        mbar_arrive_tx(barQFull(qb), Lay::kTileBytes);
+        const int qrow = tile.seq_start + tile.tl * kRows;
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
-          tma_load_2d(dst + c * Lay::kChunkBytes, &tk, hk * D + c * 64,
-                      tile.seq_start + n * kCols, barFull(s));
-        issued = n + 1;
+          tma_load_2d(sb + Lay::kQ + qb * Lay::kTileBytes + c * Lay::kChunkBytes, &tq,
+                      h * D + c * 64, qrow, barQFull(qb));
+        nq = r + 1;
+        for (int n = 0; n < n_ct; ++n, ++kt) {
+          const int s = kt % NS;
+          if (!mbar_wait(barEmpty(s), ((kt / NS) & 1) ^ 1, p.err)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_tx(barFull(s), Lay::kTileBytes);
+          const uint32_t dst = sb + Lay::kK + s * Lay::kTileBytes;
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_2d(dst + c * Lay::kChunkBytes, &tk, hk * D + c * 64,
+                        tile.seq_start + n * kCols, barFull(s));
+        }
       }
-      // drain: copies still in flight complete before the CTA may exit
-      for (int n = (issued > NS ? issued - NS : 0); n < issued; ++n)
-        mbar_wait(barFull(n % NS), (n / NS) & 1, nullptr);
-      mbar_wait(barQ, 0, nullptr);
+      // drain: copies still in flight complete before the CTA may exit (each
+      // wait is on the latest use of its barrier, so its phase is the one of
+      // that copy)
+      for (int t = (kt > NS ? kt - NS : 0); t < kt; ++t)
+        mbar_wait(barFull(t % NS), (t / NS) & 1, nullptr);
+      for (int r = (nq > 2 ? nq - 2 : 0); r < nq; ++r)
+        mbar_wait(barQFull(r & 1), (r >> 1) & 1, nullptr);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(kRows, kCols, false, false);
-      bool ok = mbar_wait(barQ, 0, p.err);
-      for (int n = 0; ok && n < n_ct; ++n) {
-        const int s = n % NS, b = n & 1;
-        if (!mbar_wait(barFull(s), (n / NS) & 1, p.err) ||
-            !mbar_wait(barSEmpty(b), ((n >> 1) & 1) ^ 1, p.err)) {
-          *abort_flag = 1;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t qa = sb + Lay::kQ, ka = sb + Lay::kK + s * Lay::kTileBytes;
+      int kt = 0, st = 0;
+      bool ok = true;
+      for (int r = 0; ok; ++r) {
+        const int idx = item_of(r, n_items);
+        if (idx < 0) break;
+        const RowTile tile = p.tiles[idx / p.H_s];
+        const int n_ct = p.causal ? tile.tl + 1 : (tile.L + kCols - 1) / kCols;
+        const int qb = r & 1;
+        if (!mbar_wait(barQFull(qb), (r >> 1) & 1, p.err)) break;
+        const uint32_t qa = sb + Lay::kQ + qb * Lay::kTileBytes;
+        for (int n = 0; n < n_ct; ++n, ++kt, ++st) {
+          const int s = kt % NS, b = st & 1;
+          if (!mbar_wait(barFull(s), (kt / NS) & 1, p.err) ||
+              !mbar_wait(barSEmpty(b), ((st >> 1) & 1) ^ 1, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t ka = sb + Lay::kK + s * Lay::kTileBytes;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * Lay::kChunkBytes + (kk & 3) * 32;
-          tc_mma(tmem + b * kCols, sdesc_sw128(qa + off, 16, 1024),
-                 sdesc_sw128(ka + off, 16, 1024), idesc, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * Lay::kChunkBytes + (kk & 3) * 32;
+            tc_mma(tmem + b * kCols, sdesc_sw128(qa + off, 16, 1024),
+                   sdesc_sw128(ka + off, 16, 1024), idesc, kk > 0 ? 1u : 0u);
+          }
+          tc_commit(barEmpty(s));
+          tc_commit(barSFull(b));
         }
-        tc_commit(barEmpty(s));
-        tc_commit(barSFull(b));
+        tc_commit(barQEmpty(qb));
       }
       tc_commit(barDone);
       mbar_wait(barDone, 0, nullptr);
@@ -221,125 +260,137 @@ __global__ void __launch_bounds__(StatWarps<BLK>::kThreads, 1)
     const int wq = warp & 3;
     const int half = (BLK == 64) ? ((warp - 2) >> 2) : 0;
     const int row = wq * 32 + lane;
-    const int row_local = tile.tl * kRows + row;
-    const bool row_ok = row_local < tile.L;
     const uint32_t trow = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     const uint32_t partcol = kPartCol + half * 128;  // this warp's per-block partials
     const float sc = p.scale_log2;
-    float mtrue = -INFINITY, ref = -INFINITY, lsum = 0.f;
-    int nblk = 0;
-    bool ok = true;
-    for (int n = 0; n < n_ct; ++n) {
-      const int b = n & 1;
-      if (!warp_wait(barSFull(b), (n >> 1) & 1, p.err)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      float x[kW];
-      {
-        uint32_t* r = reinterpret_cast<uint32_t*>(x);
+    float* red = reinterpret_cast<float*>(smem + Lay::kRed);
+    float* xs = reinterpret_cast<float*>(smem + Lay::kX);
+    int st = 0;
+    for (int r = 0;; ++r) {
+      const int idx = item_of(r, n_items);
+      if (idx < 0) break;
+      const RowTile tile = p.tiles[idx / p.H_s];
+      const int h = idx % p.H_s;
+      const int n_ct = p.causal ? tile.tl + 1 : (tile.L + kCols - 1) / kCols;
+      const int row_local = tile.tl * kRows + row;
+      const bool row_ok = row_local < tile.L;
+      float mtrue = -INFINITY, ref = -INFINITY, lsum = 0.f;
+      int nblk = 0;
+      bool ok = true;
+      for (int n = 0; n < n_ct; ++n, ++st) {
+        const int b = st & 1;
+        if (!warp_wait(barSFull(b), (st >> 1) & 1, p.err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        float x[kW];
+        {
+          uint32_t* rr = reinterpret_cast<uint32_t*>(x);
 #pragma unroll
-        for (int c = 0; c < kW; c += 32) tmem_ld32(trow + b * kCols + half * 64 + c, r + c);
-      }
-      tc_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(barSEmpty(b));
-      const int col0 = n * kCols + half * 64;
-      if (n == n_ct - 1) {  // only the last tile can cross the diagonal or the sequence end
+          for (int c = 0; c < kW; c += 32) tmem_ld32(trow + b * kCols + half * 64 + c, rr + c);
+        }
+        tc_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(barSEmpty(b));
+        const int col0 = n * kCols + half * 64;
+        if (n == n_ct - 1) {  // only the last tile can cross the diagonal or the sequence end
 #pragma unroll
-        for (int c = 0; c < kW; ++c) {
-          const int j = col0 + c;
-          if (!((j < tile.L) && (!p.causal || j <= row_local))) x[c] = -INFINITY;
+          for (int c = 0; c < kW; ++c) {
+            const int j = col0 + c;
+            if (!((j < tile.L) && (!p.causal || j <= row_local))) x[c] = -INFINITY;
+          }
+        }
+        // block max on the raw scores (scaling by sc > 0 preserves order)
+        float m0 = -INFINITY, m1 = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < kW; c += 4) {
+          m0 = fmax3(m0, x[c], x[c + 1]);
+          m1 = fmax3(m1, x[c + 2], x[c + 3]);
+        }
+        float bm = fmaxf(m0, m1) * sc;
+        if (!row_ok) bm = -INFINITY;
+        mtrue = fmaxf(mtrue, bm);
+        float alpha = 1.f;
+        if (bm > ref + kTau) {
+          alpha = (ref == -INFINITY) ? 0.f : ex2(ref - bm);
+          ref = bm;
+          lsum *= alpha;
+        }
+        if (__any_sync(0xffffffffu, alpha != 1.f) && nblk > 0) {
+          tc_wait_st();
+          rescale_parts(trow + partcol, nblk, alpha);
+        }
+        // exp2(x * sc - ref) with one packed FMA per two scores, packed sums
+        const float nrs = (ref == -INFINITY) ? 0.f : -ref;
+        const float2 sc2 = make_float2(sc, sc), nrs2 = make_float2(nrs, nrs);
+        float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int c = 0; c < kW; c += 4) {
+          float2 t0 = ffma2(make_float2(x[c], x[c + 1]), sc2, nrs2);
+          float2 t1 = ffma2(make_float2(x[c + 2], x[c + 3]), sc2, nrs2);
+          t0.x = ex2(t0.x);
+          t0.y = ex2(t0.y);
+          t1.x = ex2(t1.x);
+          t1.y = ex2(t1.y);
+          acc0 = fadd2(acc0, t0);
+          acc1 = fadd2(acc1, t1);
+        }
+        float bs = (acc0.x + acc0.y) + (acc1.x + acc1.y);
+        if (!row_ok) bs = 0.f;
+        lsum += bs;
+        tmem_st1(trow + partcol + nblk, __float_as_uint(bs));
+        ++nblk;
+      }
+      tc_wait_st();
+      // ------------------------------------------------------ item epilogue
+      // A warp whose wait gave up flags it before the barrier; every warp
+      // reads the flag after it, so all take the same exit.
+      if (!ok && lane == 0) *stat_fail = 1;
+      if (BLK == 64) {
+        xs[(half * 3 + 0) * 128 + row] = mtrue;
+        xs[(half * 3 + 1) * 128 + row] = ref;
+        xs[(half * 3 + 2) * 128 + row] = lsum;
+      }
+      named_bar(1, 32 * kSW);
+      const bool good = (*stat_fail == 0);
+      float M = mtrue, Rf = ref, Lt = lsum, own_scale = 1.f;
+      if (BLK == 64) {
+        // merge the two column halves of each row (separate lazy references)
+        const int oh = half ^ 1;
+        const float mo = xs[(oh * 3 + 0) * 128 + row], ro = xs[(oh * 3 + 1) * 128 + row],
+                    lo = xs[(oh * 3 + 2) * 128 + row];
+        M = fmaxf(mtrue, mo);
+        Rf = fmaxf(ref, ro);
+        if (Rf == -INFINITY) {
+          Lt = 0.f;
+        } else {
+          own_scale = (ref == -INFINITY) ? 0.f : ex2(ref - Rf);
+          const float other = (ro == -INFINITY) ? 0.f : ex2(ro - Rf);
+          Lt = lsum * own_scale + lo * other;
         }
       }
-      // block max on the raw scores (scaling by sc > 0 preserves order)
-      float m0 = -INFINITY, m1 = -INFINITY;
+      const float inv = (row_ok && Lt > 0.f) ? own_scale / Lt : 0.f;
+      if (good && row_ok && half == 0) {
+        const size_t o = static_cast<size_t>(h) * p.T + tile.seq_start + row_local;
+        p.row_max[o] = M * kLn2;
+        p.row_sum[o] = Lt * ex2(Rf - M);
+      }
+      for (int c0 = 0; c0 < nblk; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(trow + partcol + c0, v);
+        tc_wait_ld();
+        float f[32];
 #pragma unroll
-      for (int c = 0; c < kW; c += 4) {
-        m0 = fmax3(m0, x[c], x[c + 1]);
-        m1 = fmax3(m1, x[c + 2], x[c + 3]);
+        for (int i = 0; i < 32; ++i) f[i] = (c0 + i < nblk) ? __uint_as_float(v[i]) * inv : 0.f;
+        const float tot = transpose_reduce32(f);
+        const int k = c0 + lane;
+        if (k < nblk) red[wq * 256 + (BLK == 64 ? 2 * k + half : k)] = tot;
       }
-      float bm = fmaxf(m0, m1) * sc;
-      if (!row_ok) bm = -INFINITY;
-      mtrue = fmaxf(mtrue, bm);
-      float alpha = 1.f;
-      if (bm > ref + kTau) {
-        alpha = (ref == -INFINITY) ? 0.f : ex2(ref - bm);
-        ref = bm;
-        lsum *= alpha;
-      }
-      if (__any_sync(0xffffffffu, alpha != 1.f) && nblk > 0) {
-        tc_wait_st();
-        rescale_parts(trow + partcol, nblk, alpha);
-      }
-      // exp2(x * sc - ref) with one packed FMA per two scores, packed sums
-      const float nrs = (ref == -INFINITY) ? 0.f : -ref;
-      const float2 sc2 = make_float2(sc, sc), nrs2 = make_float2(nrs, nrs);
-      float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int c = 0; c < kW; c += 4) {
-        float2 t0 = ffma2(make_float2(x[c], x[c + 1]), sc2, nrs2);
-        float2 t1 = ffma2(make_float2(x[c + 2], x[c + 3]), sc2, nrs2);
-        t0.x = ex2(t0.x);
-        t0.y = ex2(t0.y);
-        t1.x = ex2(t1.x);
-        t1.y = ex2(t1.y);
-        acc0 = fadd2(acc0, t0);
-        acc1 = fadd2(acc1, t1);
-      }
-      float bs = (acc0.x + acc0.y) + (acc1.x + acc1.y);
-      if (!row_ok) bs = 0.f;
-      lsum += bs;
-      tmem_st1(trow + partcol + nblk, __float_as_uint(bs));
-      ++nblk;
-    }
-    tc_wait_st();
-    // -------------------------------------------------------- epilogue
-    const bool good = ok && (*abort_flag == 0);
-    float M = mtrue, Rf = ref, Lt = lsum, own_scale = 1.f;
-    if (BLK == 64) {
-      // merge the two column halves of each row (separate lazy references)
-      float* xs = reinterpret_cast<float*>(smem + Lay::kX);
-      xs[(half * 3 + 0) * 128 + row] = mtrue;
-      xs[(half * 3 + 1) * 128 + row] = ref;
-      xs[(half * 3 + 2) * 128 + row] = lsum;
+      tc_fence_before();
       named_bar(1, 32 * kSW);
-      const int oh = half ^ 1;
-      const float mo = xs[(oh * 3 + 0) * 128 + row], ro = xs[(oh * 3 + 1) * 128 + row],
-                  lo = xs[(oh * 3 + 2) * 128 + row];
-      M = fmaxf(mtrue, mo);
-      Rf = fmaxf(ref, ro);
-      if (Rf == -INFINITY) {
-        Lt = 0.f;
-      } else {
-        own_scale = (ref == -INFINITY) ? 0.f : ex2(ref - Rf);
-        const float other = (ro == -INFINITY) ? 0.f : ex2(ro - Rf);
-        Lt = lsum * own_scale + lo * other;
-      }
-    }
-    const float inv = (row_ok && Lt > 0.f) ? own_scale / Lt : 0.f;
-    if (good && row_ok && half == 0) {
-      const size_t o = static_cast<size_t>(h) * p.T + tile.seq_start + row_local;
-      p.row_max[o] = M * kLn2;
-      p.row_sum[o] = Lt * ex2(Rf - M);
-    }
-    float* red = reinterpret_cast<float*>(smem + Lay::kRed);
-    for (int c0 = 0; c0 < nblk; c0 += 32) {
-      uint32_t v[32];
-      tmem_ld32(trow + partcol + c0, v);
-      tc_wait_ld();
-      float f[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) f[i] = (c0 + i < nblk) ? __uint_as_float(v[i]) * inv : 0.f;
-      const float tot = transpose_reduce32(f);
-      const int k = c0 + lane;
-      if (k < nblk) red[wq * 256 + (BLK == 64 ? 2 * k + half : k)] = tot;
-    }
-    tc_fence_before();
-    named_bar(1, 32 * kSW);
-    if (good) {
+      if (!good) break;
       const int t0 = threadIdx.x - 64;
       const int nbt = (BLK == 64) ? 2 * nblk : nblk;  // block columns covered
       if (BLK == 64) {
@@ -361,6 +412,9 @@ __global__ void __launch_bounds__(StatWarps<BLK>::kThreads, 1)
           p.mass[static_cast<size_t>(h) * p.C + rbk.cand_off + c] = m;
         }
       }
+      // the next item rewrites xs after this item's second barrier (all xs
+      // reads are before it) and red after its own first barrier (all red
+      // reads above are before every warp's arrival there)
     }
   }
   tc_fence_before();
@@ -379,7 +433,14 @@ cudaError_t launch_stats_t(const CompressParams& p, const CUtensorMap& tq, const
   const int smem = StatsLayout<D>::kBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(p.n_tiles, p.H_s);
+  int sms = 0;
+  e = sm_count(&sms);
+  if (e != cudaSuccess) return e;
+  const long long items = static_cast<long long>(p.n_tiles) * p.H_s;
+  if (items <= 0) return cudaSuccess;
+  // persistent: one CTA per SM (the 512 TMEM columns and the shared memory
+  // allow no second one), each walking its share of the item list
+  const int grid = static_cast<int>(items < sms ? items : sms);
   kern<<<grid, StatWarps<BLK>::kThreads, smem, s>>>(tq, tk, p);
   return cudaGetLastError();
 }
