@@ -98,12 +98,12 @@ struct LayerState {
   int* tile_of = nullptr;
   int* union_cnt = nullptr;
   int* union_list = nullptr;
+  int* utile = nullptr;
   long long* nnz_dev = nullptr;
   int* col_idx = nullptr;
   uint16_t* values = nullptr;
   size_t values_bytes = 0, colidx_bytes = 0;
   CUtensorMap pmap;  // values as [(nnz+1)*B rows][B cols], 64x64 boxes (per-group retrieval)
-  CUtensorMap gmap;  // same rows, 64x1 boxes for 4-row gathers (cluster retrieval)
 };
 
 struct ProfRec {
@@ -132,6 +132,11 @@ struct mf_bsr_s {
   mf_free_fn dealloc = nullptr;
   void* ctx = nullptr;
   std::vector<LayerState> layers;
+  // team retrieval's exchange ring (allocated on first use, sized for the
+  // device's team count)
+  void* ring = nullptr;
+  uint32_t* ring_flags = nullptr;
+  int ring_teams = 0;
 };
 
 namespace {
@@ -323,6 +328,8 @@ void mf_bsr_destroy(mf_bsr_t h) {
   dev_free(h, h->tiles_d, nullptr);
   dev_free(h, h->slabs_d, nullptr);
   dev_free(h, h->err_d, nullptr);
+  dev_free(h, h->ring, nullptr);
+  dev_free(h, h->ring_flags, nullptr);
   cudaDeviceSynchronize();
   if (h->host_pinned) cudaFreeHost(h->host_pinned);
   delete h;
@@ -355,6 +362,7 @@ int mf_compress(mf_bsr_t h, int layer, const void* q, const void* k, int dtype, 
   const size_t o_tile = off; off += align_up(HC * 4);
   const size_t o_uc = off; off += align_up((size_t)h->R * 4);
   const size_t o_ul = off; off += align_up((size_t)h->C * 4);
+  const size_t o_ut = off; off += align_up(HC * 4);
   const size_t o_nnz = off; off += 256;
   L.meta = dev_alloc(h, off, s);
   if (!L.meta) return fail(MF_ERR_OOM, "allocation of %zu bytes failed", off);
@@ -369,6 +377,7 @@ int mf_compress(mf_bsr_t h, int layer, const void* q, const void* k, int dtype, 
   L.tile_of = (int*)(mb + o_tile);
   L.union_cnt = (int*)(mb + o_uc);
   L.union_list = (int*)(mb + o_ul);
+  L.utile = (int*)(mb + o_ut);
   L.nnz_dev = (long long*)(mb + o_nnz);
 
   CompressParams cp{};
@@ -394,6 +403,7 @@ int mf_compress(mf_bsr_t h, int layer, const void* q, const void* k, int dtype, 
   cp.tile_of = L.tile_of;
   cp.union_cnt = L.union_cnt;
   cp.union_list = L.union_list;
+  cp.utile = L.utile;
   cp.nnz_out = L.nnz_dev;
   cp.err = h->err_d;
 
@@ -470,8 +480,6 @@ int mf_compress(mf_bsr_t h, int layer, const void* q, const void* k, int dtype, 
   MF_CUDA(timed(h, MF_K_UNION, s, [&] { return launch_union(cp, s); }), "union kernel");
   if ((rc = make_map(&L.pmap, L.values, B, (uint64_t)(cap + 1) * B, (uint64_t)B * 2, 64, 64)) != MF_OK)
     return rc;
-  if ((rc = make_map(&L.gmap, L.values, B, (uint64_t)(cap + 1) * B, (uint64_t)B * 2, 64, 1)) != MF_OK)
-    return rc;
   L.valid = true;
   L.dtype = dtype;
   L.d = d;
@@ -521,6 +529,7 @@ int mf_retrieve(mf_bsr_t h, const float* W, const void* v, void* o, int dtype, i
     rp.tile_of = L.tile_of;
     rp.union_cnt = L.union_cnt;
     rp.union_list = L.union_list;
+    rp.utile = L.utile;
     rp.W = W + (size_t)x * H_r * h->H_s;
     rp.zero_tile = (int)L.capacity;
     rp.values = L.values;
@@ -531,10 +540,27 @@ int mf_retrieve(mf_bsr_t h, const float* W, const void* v, void* o, int dtype, i
       CUtensorMap tv{};
       int rc = make_map(&tv, vx, (uint64_t)H_kv * d, h->T, (uint64_t)H_kv * d * 2, 64, 64);
       if (rc != MF_OK) return rc;
-      if (retrieve_cluster_supported(h->H_s, H_r, H_kv, d, h->B)) {
+      if (retrieve_team_supported(h->H_s, H_r, H_kv, d, h->B)) {
+        int sms = 0;
+        MF_CUDA(sm_count(&sms), "device query");
+        const int teams = retrieve_team_count(h->n_slabs, sms);
+        if (!h->ring) {
+          const int cap = retrieve_team_count(1 << 30, sms);
+          h->ring = dev_alloc(h, retrieve_team_ring_bytes(cap), s);
+          h->ring_flags = (uint32_t*)dev_alloc(h, retrieve_team_flag_bytes(cap), s);
+          if (!h->ring || !h->ring_flags) return fail(MF_ERR_OOM, "exchange ring allocation failed");
+          h->ring_teams = cap;
+        }
+        CUtensorMap ta{};
+        rc = make_map(&ta, h->ring, 64, (uint64_t)retrieve_team_ring_rows(h->ring_teams), 128, 64,
+                      (uint32_t)retrieve_team_ring_box_rows(H_r));
+        if (rc != MF_OK) return rc;
+        MF_CUDA(cudaMemsetAsync(h->ring_flags, 0, retrieve_team_flag_bytes(teams), s), "ring reset");
         MF_CUDA(timed(h, MF_K_RETRIEVE, s,
-                      [&] { return launch_retrieve_cluster(rp, L.gmap, tv, ox, s); }),
-                "retrieval kernel (cluster)");
+                      [&] {
+                        return launch_retrieve_team(rp, ta, tv, ox, h->ring, h->ring_flags, teams, s);
+                      }),
+                "retrieval kernel (team)");
       } else {
         MF_CUDA(timed(h, MF_K_RETRIEVE, s,
                       [&] { return launch_retrieve_bf16(rp, L.pmap, tv, ox, s); }),

@@ -50,6 +50,7 @@ struct CompressParams {
   int* tile_of;     // [C][H_s]  tile index of (block-row cand, head) or -1
   int* union_cnt;   // [R]
   int* union_list;  // [C]
+  int* utile;       // [C][H_s]  tile_of in union order: row cand_off + j is union column j
   long long* nnz_out;  // device scalar
   int* err;
 };
@@ -63,6 +64,7 @@ struct RetrieveParams {
   const int* tile_of;     // [C][H_s]
   const int* union_cnt;   // [R]
   const int* union_list;  // [C]
+  const int* utile;       // [C][H_s] tile_of in union order
   const float* W;         // [H_r][H_s] of this receiver layer
   int zero_tile;          // index of an all-zero tile (= nnz)
   const uint16_t* values; // [nnz+1][B][B] bf16 tiles
@@ -102,9 +104,20 @@ cudaError_t launch_pack_f32(const CompressParams& p, const float* q, const float
 cudaError_t launch_union(const CompressParams& p, cudaStream_t s);
 cudaError_t launch_retrieve_bf16(const RetrieveParams& p, const CUtensorMap& tp,
                                  const CUtensorMap& tv, void* o, cudaStream_t s);
-bool retrieve_cluster_supported(int H_s, int H_r, int H_kv, int d, int B);
-cudaError_t launch_retrieve_cluster(const RetrieveParams& p, const CUtensorMap& tp,
-                                    const CUtensorMap& tv, void* o, cudaStream_t s);
+// Team retrieval: persistent cooperative kernel, teams of 8 CTAs exchanging
+// the combined maps through a ring in global memory (`ring` of
+// retrieve_team_ring_bytes, `flags` of retrieve_team_flag_bytes, zeroed
+// before every launch; `ta` maps the ring as retrieve_team_ring_rows x 64 bf16
+// with boxes of 64 x retrieve_team_ring_box_rows).
+bool retrieve_team_supported(int H_s, int H_r, int H_kv, int d, int B);
+int retrieve_team_count(int n_slabs, int sms);
+size_t retrieve_team_ring_bytes(int n_teams);
+size_t retrieve_team_flag_bytes(int n_teams);
+int retrieve_team_ring_box_rows(int H_r);
+int retrieve_team_ring_rows(int n_teams);
+cudaError_t launch_retrieve_team(const RetrieveParams& p, const CUtensorMap& ta,
+                                 const CUtensorMap& tv, void* o, void* ring, uint32_t* flags,
+                                 int n_teams, cudaStream_t s);
 cudaError_t launch_retrieve_f32(const RetrieveParams& p, const uint16_t* values, const float* v,
                                 float* o, cudaStream_t s);
 

@@ -87,9 +87,6 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t sr
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
-__device__ __forceinline__ void bulk_wait_read_all() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
 __device__ __forceinline__ void bulk_wait_read_1() {
   asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
@@ -174,18 +171,8 @@ __device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v)
                : "memory");
 }
-__device__ __forceinline__ void tmem_st2(uint32_t taddr, uint32_t v0, uint32_t v1) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1,%2};" ::"r"(taddr), "r"(v0),
-               "r"(v1)
-               : "memory");
-}
 __device__ __forceinline__ void tmem_ld1(uint32_t taddr, uint32_t& v) {
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(v) : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_ld2(uint32_t taddr, uint32_t& v0, uint32_t& v1) {
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0,%1}, [%2];"
-               : "=r"(v0), "=r"(v1)
-               : "r"(taddr));
 }
 
 // Shared-memory matrix descriptor (tcgen05 form): start address, leading and
@@ -211,85 +198,43 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_ma
          ((uint32_t)(M >> 4) << 24);
 }
 
-// ---------------------------------------------------- clusters and DSMEM --
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
+// ------------------------------------------- signalling through global memory --
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* ptr) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+  return v;
 }
-// Address of the same shared-memory offset in CTA `cta` of this cluster.
-__device__ __forceinline__ uint32_t mapa(uint32_t saddr, uint32_t cta) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(cta));
-  return r;
+// Orders this thread's generic-proxy view of global memory before its later
+// async-proxy (TMA) accesses.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
 }
-__device__ __forceinline__ void st_cluster_v4(uint32_t raddr, uint4 v) {
-  asm volatile("st.shared::cluster.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(raddr), "r"(v.x), "r"(v.y),
-               "r"(v.z), "r"(v.w)
-               : "memory");
-}
-// Asynchronous 16-byte store into another CTA's shared memory; on completion
-// it counts 16 transaction bytes on that CTA's mbarrier `rbar`.
-__device__ __forceinline__ void st_async_v4(uint32_t raddr, uint4 v, uint32_t rbar) {
-  asm volatile(
-      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1,%2,%3,%4}, [%5];" ::"r"(
-          raddr),
-      "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(rbar)
-      : "memory");
-}
-// Arrive on an mbarrier of another CTA of the cluster, releasing this
-// thread's earlier writes at cluster scope.
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t raddr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(raddr)
-               : "memory");
-}
-__device__ __forceinline__ bool mbar_try_cluster(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Bounded wait that acquires at cluster scope (arrivals from other CTAs).
-__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, int* err,
-                                                  unsigned long long limit_ns = kWaitLimitNs) {
-  if (mbar_try_cluster(bar, parity)) return true;
+// Bounded wait until the counter at `ptr` reaches `target` (acquire); false
+// on timeout.
+__device__ __forceinline__ bool wait_counter(const uint32_t* ptr, uint32_t target, int* err,
+                                             unsigned long long limit_ns = kWaitLimitNs) {
+  if (ld_acquire_gpu(ptr) >= target) return true;
   const unsigned long long t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_cluster(bar, parity)) return true;
-    if ((it & 63u) == 0 && globaltimer() - t0 > limit_ns) {
+    if (ld_acquire_gpu(ptr) >= target) return true;
+    if ((it & 15u) == 0 && globaltimer() - t0 > limit_ns) {
       set_error(err, kDevErrTimeout);
       return false;
     }
+    __nanosleep(32);
   }
 }
-// tcgen05.commit whose arrival goes to the same-offset mbarrier of every CTA
-// in `mask`.
-__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(bar),
-      "h"(mask)
-      : "memory");
+__device__ __forceinline__ void red_relaxed_gpu_add(uint32_t* ptr, uint32_t v) {
+  asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
 }
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
-                   : "memory");
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
 }
-// TMA gather of four 1-row boxes (rows y0..y3 at column x) into 4 consecutive
-// box rows of shared memory.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int x, int y0,
-                                            int y1, int y2, int y3, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-      "l"(map), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar)
-      : "memory");
+// Fetch [ptr, ptr + bytes) into L2 (bytes a multiple of 16, ptr 16-aligned).
+__device__ __forceinline__ void prefetch_l2(const void* ptr, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
 }
+
 // 16-byte asynchronous global->shared copy (L2 only); src_bytes = 0 writes
 // zeros without reading global memory.
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
@@ -300,11 +245,6 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32
 // barrier's expected count includes this arrival).
 __device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-  uint32_t r;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
-  return r;
 }
 
 // ------------------------------------------------------------ small math --

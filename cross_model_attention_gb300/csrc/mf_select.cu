@@ -20,6 +20,7 @@
 //                   one shared-memory pass over warp totals)
 //   union_kernel    per block-row, the ascending union over sender heads of
 //                   the kept block columns (the retrieval's iteration list)
+//                   and the kept-tile table re-indexed by union position
 #include "mf_internal.cuh"
 #include "mf_ptx.cuh"
 
@@ -203,6 +204,14 @@ __global__ void __launch_bounds__(256) union_kernel(const CompressParams p) {
   for (int i = threadIdx.x; i < n; i += blockDim.x)
     if (flag[i]) p.union_list[rbk.cand_off + pos[i] - 1] = i;
   if (threadIdx.x == 0) p.union_cnt[rb] = (n > 0) ? pos[n - 1] : 0;
+  // the kept tiles again, in union order, so that a consumer walking the
+  // union needs one independent load per block instead of two dependent ones
+  for (int x = threadIdx.x; x < n * p.H_s; x += blockDim.x) {
+    const int i = x / p.H_s, hh = x - i * p.H_s;
+    if (flag[i])
+      p.utile[static_cast<size_t>(rbk.cand_off + pos[i] - 1) * p.H_s + hh] =
+          p.tile_of[static_cast<size_t>(rbk.cand_off + i) * p.H_s + hh];
+  }
 }
 
 // One thread waits on an mbarrier that expects one arrival nobody makes; the

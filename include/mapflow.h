@@ -175,7 +175,12 @@ MF_API int mf_compress(mf_bsr_t h, int layer, const void* q, const void* k, int 
  * O_i[t] = sum over the kept blocks (h, bi, bj) of block-row bi of t:
  *          W[i,h] * P_h[t, bj cols] @ V_g(i)[bj rows], fp32 accumulation.
  * Rows of blocks with no kept tile get O = 0.  Asynchronous.
- * Errors: MF_ERR_ARG, MF_ERR_UNSUPPORTED, MF_ERR_STATE, MF_ERR_CUDA.
+ * With 8 KV heads and H_r <= 32 (bf16) the kernel is a cooperative launch
+ * whose CTAs pass partial results through a small exchange ring owned by the
+ * handle (about 20 MB, allocated with the handle's allocator on the first such
+ * call, on `stream`): calls of one handle must therefore not run concurrently
+ * on different streams.
+ * Errors: MF_ERR_ARG, MF_ERR_UNSUPPORTED, MF_ERR_STATE, MF_ERR_CUDA, MF_ERR_OOM.
  */
 MF_API int mf_retrieve(mf_bsr_t h, const float* W, const void* v, void* o, int dtype,
                 int H_r, int H_kv, int d, const int32_t* layer_map_host, int n,
