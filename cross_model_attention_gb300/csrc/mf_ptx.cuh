@@ -241,6 +241,10 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
                : "memory");
 }
+// 4-byte asynchronous global->shared copy (through L1).
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
 // Arrive on `bar` once this thread's earlier cp.async copies have landed (the
 // barrier's expected count includes this arrival).
 __device__ __forceinline__ void cp_async_arrive(uint32_t bar) {

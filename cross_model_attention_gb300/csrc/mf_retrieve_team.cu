@@ -40,7 +40,7 @@
 //
 // Warp roles (512 threads): warp 0 TMA loads of V and of the group's A_hat^T,
 // warps 11-14 copy sender rows with 16-byte cp.async straight into the
-// swizzled operand layout (after prefetching them into L2 four blocks ahead),
+// swizzled operand layout (their tile indices arrive four blocks ahead),
 // warp 1 issues the combine MMAs, warps 2-9 convert and store A_hat and write
 // each slab's output, warp 10 issues the A_hat.V MMAs, warp 15 publishes
 // stored blocks.  Every wait, on a shared-memory barrier or a global counter,
@@ -60,7 +60,8 @@ constexpr int kNComb = 32;      // combine N: 8 groups x 4 head slots
 constexpr int kRing = 4;        // global ring slots per team
 constexpr int kASlots = 2;      // A_hat^T tiles staged in shared memory
 constexpr int kSlotHeads = 4;   // head slots per group
-constexpr int kPrefetch = 4;    // blocks of sender rows fetched into L2 ahead of the copies
+constexpr int kIdxSlots = 8;    // tile-index ring of the copy warps (blocks)
+constexpr int kIdxAhead = 4;    // blocks whose tile indices are requested ahead of the copies
 constexpr int kMaxSlabs = 128;  // slab records of a team kept in shared memory
 constexpr int kGroupElems = kSlotHeads * 64 * 64;  // one group's A_hat in a ring slot
 
@@ -71,30 +72,32 @@ struct SlabRec {
 
 struct TeamLayout {
   int hpad, nslice, pairs, abuf, vbytes, nv;
-  int off_p, off_a, off_v, off_w, off_s, off_bar, bytes;
+  int off_p, off_a, off_v, off_w, off_s, off_i, off_bar, bytes;
   __host__ __device__ TeamLayout(int D, int Hs, int hpc) {
     hpad = (Hs + 15) / 16 * 16;
     nslice = hpad / 16;
     pairs = (hpc + 1) / 2;
     abuf = kGroupElems * 2;
     vbytes = 64 * D * 2;
-    const int base = kPSlots * kSliceBytes + kASlots * abuf + 4096 + kMaxSlabs * 32;
+    const int base = kPSlots * kSliceBytes + kASlots * abuf + 4096 + kMaxSlabs * 32 + kIdxSlots * 256;
     nv = (base + 2 * vbytes + 2048 <= 226 * 1024) ? 2 : 1;
     off_p = 0;
     off_a = off_p + kPSlots * kSliceBytes;
     off_v = off_a + kASlots * abuf;
     off_w = off_v + nv * vbytes;
     off_s = off_w + 4096;
-    off_bar = off_s + kMaxSlabs * 32;
-    bytes = off_bar + 32 * 8 + 64 + 1024;
+    off_i = off_s + kMaxSlabs * 32;
+    off_bar = off_i + kIdxSlots * 256;
+    bytes = off_bar + 48 * 8 + 64 + 1024;
   }
 };
 
 enum : int {
   kBarVFull = 0, kBarVEmpty = 2, kBarDFull = 4, kBarDEmpty = 6, kBarAFull = 8, kBarAEmpty = 10,
   kBarO = 12, kBarOFree = 13, kBarStored = 14, kBarPFull = 14 + kRing,
-  kBarPEmpty = kBarPFull + kPSlots, kNumBars = kBarPEmpty + kPSlots
+  kBarPEmpty = kBarPFull + kPSlots, kBarIdx = kBarPEmpty + kPSlots, kNumBars = kBarIdx + kIdxSlots
 };
+static_assert(kNumBars <= 48, "barrier area");
 
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int* err) {
   int ok = 1;
@@ -210,6 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(kBarO), 1);
     mbar_init(bar(kBarOFree), 8);
     for (int s = 0; s < kRing; ++s) mbar_init(bar(kBarStored + s), 8);
+    for (int s = 0; s < kIdxSlots; ++s) mbar_init(bar(kBarIdx + s), kPThreads);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -286,49 +290,47 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t dst0 = sb + lay.off_p + (hl >> 3) * 1024 + sw128_off(hl & 7, cg);
     const size_t row_bytes = static_cast<size_t>(BLK) * 2;
     const char* vbase = reinterpret_cast<const char*>(p.values);
-    // L2 prefetch of the rows of the block kPrefetch ahead: thread t < H_s
-    // takes head t (8 rows of its tile, both 64-column halves when B = 128).
-    // The tile index (one load from the union-ordered table) is read one
-    // step before the prefetch is issued, so it never stalls the copies.
-    BlockCursor pc;
-    cursor_settle<kSub>(pc, tab, p, team, n_teams);
-    int pf_tt = -1, pf_rowoff = 0;
-    auto prefetch_next = [&]() {
-      if (pf_tt >= 0)
-        prefetch_l2(vbase + (static_cast<size_t>(pf_tt) * BLK + pf_rowoff) * row_bytes,
-                    static_cast<uint32_t>(8 * row_bytes));
-      pf_tt = -1;
-      if (pc.done) return;
-      if (pc.j % kSub == 0 && t < p.H_s) {
-        pf_tt = p.utile[static_cast<size_t>(pc.s.cand_off + pc.j / kSub) * p.H_s + t];
-        pf_rowoff = pc.s.half * 64 + 8 * g;
-      }
-      ++pc.j;
-      cursor_settle<kSub>(pc, tab, p, team, n_teams);
+    // Tile indices come through a shared-memory ring filled by cp.async
+    // kIdxAhead blocks ahead (thread t < H_s copies head t's entry of the
+    // union-ordered table), so no copy waits on a global load.  A slot is
+    // rewritten kIdxSlots - kIdxAhead blocks after its use; the copy warps
+    // cannot drift that far apart (a block's copies need every warp's
+    // arrivals on the previous blocks' slices).
+    const int* idx_ring = reinterpret_cast<const int*>(smem + lay.off_i);
+    BlockCursor ic;
+    cursor_settle<kSub>(ic, tab, p, team, n_teams);
+    int n_req = 0;
+    auto request_next = [&]() {
+      if (ic.done) return;
+      const int slot = n_req % kIdxSlots;
+      if (t < p.H_s)
+        cp_async4(sb + lay.off_i + slot * 256 + t * 4,
+                  p.utile + static_cast<size_t>(ic.s.cand_off + ic.j / kSub) * p.H_s + t);
+      cp_async_arrive(bar(kBarIdx + slot));
+      ++n_req;
+      ++ic.j;
+      cursor_settle<kSub>(ic, tab, p, team, n_teams);
     };
-    for (int i = 0; i <= kPrefetch; ++i) prefetch_next();
+    for (int i = 0; i < kIdxAhead; ++i) request_next();
     bool ok = true;
-    int slot = 0;
+    int slot = 0, u = 0;
     for (int r = 0; ok; ++r) {
       const SlabRec sr = slab_rec<kSub>(r, tab, p, team, n_teams);
       if (sr.n_sub < 0) break;
-      int nxt[4];
-      auto fetch = [&](int j, int (&o4)[4]) {
-        const int* trow = p.utile + static_cast<size_t>(sr.cand_off + j / kSub) * p.H_s;
+      for (int j = 0; ok && j < sr.n_sub; ++j, ++u) {
+        const int cs = j % kSub;
+        request_next();
+        if (!warp_wait(bar(kBarIdx + u % kIdxSlots), (u / kIdxSlots) & 1, p.err)) {
+          ok = false;
+          break;
+        }
+        const int* irow = idx_ring + (u % kIdxSlots) * 64;
+        int tix[4];
 #pragma unroll
         for (int sl = 0; sl < 4; ++sl) {
           const int h = sl * 16 + hl;
-          o4[sl] = (sl < lay.nslice && h < p.H_s) ? trow[h] : -1;
+          tix[sl] = (sl < lay.nslice && h < p.H_s) ? irow[h] : -1;
         }
-      };
-      if (sr.n_sub > 0) fetch(0, nxt);
-      for (int j = 0; ok && j < sr.n_sub; ++j) {
-        const int cs = j % kSub;
-        prefetch_next();
-        int tix[4];
-#pragma unroll
-        for (int sl = 0; sl < 4; ++sl) tix[sl] = nxt[sl];
-        if (j + 1 < sr.n_sub) fetch(j + 1, nxt);
 #pragma unroll
         for (int sl = 0; sl < 4; ++sl) {
           if (sl >= lay.nslice || !ok) continue;
