@@ -54,8 +54,9 @@ namespace {
 constexpr int kTeam = 8;        // CTAs per team = receiver KV groups
 constexpr int kThreads = 512;   // warp 0 loads, 1 combine MMA, 2-9 convert, 10 A_hat.V MMA, 11-14 P copies, 15 signals
 constexpr int kPThreads = 128;  // P copy threads (warps 11-14)
-constexpr int kPSlots = 6;      // P ring: 16-head slices of 8 rows x 64 columns (16 KB)
+constexpr int kPBytes = 96 * 1024;  // P ring: whole blocks of 16-head slices (8 rows x 64 columns, 16 KB)
 constexpr int kSliceBytes = 8 * 16 * 128;
+constexpr int kPBMax = 3;       // block slots of the P ring at most
 constexpr int kNComb = 32;      // combine N: 8 groups x 4 head slots
 constexpr int kRing = 4;        // global ring slots per team
 constexpr int kASlots = 2;      // A_hat^T tiles staged in shared memory
@@ -71,18 +72,20 @@ struct SlabRec {
 };
 
 struct TeamLayout {
-  int hpad, nslice, pairs, abuf, vbytes, nv;
+  int hpad, nslice, npb, pairs, abuf, vbytes, nv;
   int off_p, off_a, off_v, off_w, off_s, off_i, off_bar, bytes;
   __host__ __device__ TeamLayout(int D, int Hs, int hpc) {
     hpad = (Hs + 15) / 16 * 16;
     nslice = hpad / 16;
+    npb = kPBytes / (nslice * kSliceBytes);
+    if (npb > kPBMax) npb = kPBMax;
     pairs = (hpc + 1) / 2;
     abuf = kGroupElems * 2;
     vbytes = 64 * D * 2;
-    const int base = kPSlots * kSliceBytes + kASlots * abuf + 4096 + kMaxSlabs * 32 + kIdxSlots * 256;
+    const int base = kPBytes + kASlots * abuf + 4096 + kMaxSlabs * 32 + kIdxSlots * 256;
     nv = (base + 2 * vbytes + 2048 <= 226 * 1024) ? 2 : 1;
     off_p = 0;
-    off_a = off_p + kPSlots * kSliceBytes;
+    off_a = off_p + kPBytes;
     off_v = off_a + kASlots * abuf;
     off_w = off_v + nv * vbytes;
     off_s = off_w + 4096;
@@ -95,7 +98,7 @@ struct TeamLayout {
 enum : int {
   kBarVFull = 0, kBarVEmpty = 2, kBarDFull = 4, kBarDEmpty = 6, kBarAFull = 8, kBarAEmpty = 10,
   kBarO = 12, kBarOFree = 13, kBarStored = 14, kBarPFull = 14 + kRing,
-  kBarPEmpty = kBarPFull + kPSlots, kBarIdx = kBarPEmpty + kPSlots, kNumBars = kBarIdx + kIdxSlots
+  kBarPEmpty = kBarPFull + kPBMax, kBarIdx = kBarPEmpty + kPBMax, kNumBars = kBarIdx + kIdxSlots
 };
 static_assert(kNumBars <= 48, "barrier area");
 
@@ -198,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   SlabRec* tab = reinterpret_cast<SlabRec*>(smem + lay.off_s);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kPSlots; ++s) {
+    for (int s = 0; s < kPBMax; ++s) {
       mbar_init(bar(kBarPFull + s), kPThreads);
       mbar_init(bar(kBarPEmpty + s), 1);
     }
@@ -217,6 +220,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
+  // zero the P ring: the lines of padded heads (beyond H_s in the last
+  // slice) are never copied and must hold finite values (their weights are 0)
+  for (int i = threadIdx.x; i < kPBytes / 16; i += kThreads)
+    *reinterpret_cast<uint4*>(smem + lay.off_p + i * 16) = make_uint4(0u, 0u, 0u, 0u);
   // the team's slab records
   for (int r = threadIdx.x; r < kMaxSlabs; r += kThreads) tab[r] = load_slab<kSub>(r, p, team, n_teams);
   // W^T as the combine's B operand: row n = 4 * group + head slot (32 rows;
@@ -313,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     for (int i = 0; i < kIdxAhead; ++i) request_next();
     bool ok = true;
-    int slot = 0, u = 0;
+    int u = 0;
     for (int r = 0; ok; ++r) {
       const SlabRec sr = slab_rec<kSub>(r, tab, p, team, n_teams);
       if (sr.n_sub < 0) break;
@@ -331,30 +338,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int h = sl * 16 + hl;
           tix[sl] = (sl < lay.nslice && h < p.H_s) ? irow[h] : -1;
         }
+        // the block slot of block u - npb has been consumed
+        const int pb = u % lay.npb;
+        int good = 1;
+        if (lane == 0) good = mbar_wait(bar(kBarPEmpty + pb), ((u / lay.npb) & 1) ^ 1, p.err) ? 1 : 0;
+        good = __shfl_sync(0xffffffffu, good, 0);
+        if (!good) {
+          ok = false;
+          break;
+        }
 #pragma unroll
         for (int sl = 0; sl < 4; ++sl) {
-          if (sl >= lay.nslice || !ok) continue;
-          const int st = slot % kPSlots;
-          const uint32_t ph = (slot / kPSlots) & 1;
-          ++slot;
-          int good = 1;
-          if (lane == 0) good = mbar_wait(bar(kBarPEmpty + st), ph ^ 1, p.err) ? 1 : 0;
-          good = __shfl_sync(0xffffffffu, good, 0);
-          if (!good) {
-            ok = false;
-            continue;
-          }
+          if (sl >= lay.nslice || sl * 16 + hl >= p.H_s) continue;  // padded heads stay zero
           const int tt = tix[sl];
           const char* src = vbase +
                             (static_cast<size_t>(tt >= 0 ? tt : 0) * BLK + sr.half * 64 + 8 * g) *
                                 row_bytes +
                             cs * 128 + cg * 16;
-          const uint32_t nbytes = tt >= 0 ? 16u : 0u;
-          const uint32_t dst = dst0 + st * kSliceBytes;
+          const uint32_t nbytes = tt >= 0 ? 16u : 0u;  // a dropped head is zero-filled
+          const uint32_t dst = dst0 + (pb * lay.nslice + sl) * kSliceBytes;
 #pragma unroll
           for (int rr = 0; rr < 8; ++rr) cp_async16(dst + rr * 2048, src + rr * row_bytes, nbytes);
-          cp_async_arrive(bar(kBarPFull + st));
         }
+        cp_async_arrive(bar(kBarPFull + pb));
       }
     }
     if (!ok && lane == 0) *abort_flag = 1;
@@ -363,26 +369,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_comb = idesc_bf16_f32(128, kNComb, true, false);
       bool ok = true;
-      int slot = 0, u = 0;
+      int u = 0;
       for (int r = 0; ok; ++r) {
         const SlabRec sr = slab_rec<kSub>(r, tab, p, team, n_teams);
         if (sr.n_sub < 0) break;
         for (int j = 0; ok && j < sr.n_sub; ++j, ++u) {
-          const int b = u & 1;
-          if (!mbar_wait(bar(kBarDEmpty + b), ((u >> 1) & 1) ^ 1, p.err)) {
+          const int b = u & 1, pb = u % lay.npb;
+          if (!mbar_wait(bar(kBarDEmpty + b), ((u >> 1) & 1) ^ 1, p.err) ||
+              !mbar_wait(bar(kBarPFull + pb), (u / lay.npb) & 1, p.err)) {
             ok = false;
             break;
           }
+          fence_async_smem();  // rows were written by cp.async (generic proxy)
+          tc_fence_after();
           const uint32_t wbase = sb + lay.off_w;
-          for (int sl = 0; sl < lay.nslice; ++sl, ++slot) {
-            const int st = slot % kPSlots;
-            if (!mbar_wait(bar(kBarPFull + st), (slot / kPSlots) & 1, p.err)) {
-              ok = false;
-              break;
-            }
-            fence_async_smem();  // rows were written by cp.async (generic proxy)
-            tc_fence_after();
-            const uint32_t pbase = sb + lay.off_p + st * kSliceBytes;
+          for (int sl = 0; sl < lay.nslice; ++sl) {
+            const uint32_t pbase = sb + lay.off_p + (pb * lay.nslice + sl) * kSliceBytes;
             const uint64_t bd = sdesc_sw128(wbase + sl * 32, 16, 1024);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
@@ -390,9 +392,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint64_t ad = sdesc_sw128(pbase + 2 * k * 2048, 2048, 1024);
               tc_mma(tmem + b * 128 + k * kNComb, ad, bd, idesc_comb, sl > 0 ? 1u : 0u);
             }
-            tc_commit(bar(kBarPEmpty + st));
           }
-          if (!ok) break;
+          tc_commit(bar(kBarPEmpty + pb));
           tc_commit(bar(kBarDFull + b));
         }
       }
