@@ -102,7 +102,7 @@ def traffic_for(kernel: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
     on the current source of that kernel; else None."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
-    src = {"stats": "mf_stats_tc.cu", "pack": "mf_pack_tc.cu", "retrieve": "mf_retrieve_tc.cu"}[kernel]
+    src = {"stats": "mf_stats_tc.cu", "pack": "mf_pack_tc.cu", "retrieve": "mf_retrieve_team.cu"}[kernel]
     with open(os.path.join(ROOT, "cross_model_attention_gb300", "csrc", src), "rb") as fh:
         sha = hashlib.sha256(fh.read()).hexdigest()[:16]
     if not os.path.exists(path):
