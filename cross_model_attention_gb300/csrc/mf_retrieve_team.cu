@@ -33,7 +33,7 @@
 //     64 keys) and V_c and accumulates O[(head, row), d] += A_hat . V_c on
 //     tcgen05 (two heads x 64 rows per M = 128 tile, N = d) into TMEM over the
 //     slab's blocks, then bumps the slot's freed counter.
-// The ring (4 slots per team) lives in L2 between its write and its reads;
+// The ring (6 slots per team) lives in L2 between its write and its reads;
 // every sender-tile byte is read from HBM once.  Slabs go to teams heaviest
 // first in a snake order; within a team all CTAs walk the same slab list,
 // whose records are staged in shared memory at the start.
@@ -58,7 +58,7 @@ constexpr int kPBytes = 96 * 1024;  // P ring: whole blocks of 16-head slices (8
 constexpr int kSliceBytes = 8 * 16 * 128;
 constexpr int kPBMax = 3;       // block slots of the P ring at most
 constexpr int kNComb = 32;      // combine N: 8 groups x 4 head slots
-constexpr int kRing = 4;        // global ring slots per team
+constexpr int kRing = 6;        // global ring slots per team
 constexpr int kASlots = 2;      // A_hat^T tiles staged in shared memory
 constexpr int kSlotHeads = 4;   // head slots per group
 constexpr int kIdxSlots = 8;    // tile-index ring of the copy warps (blocks)

@@ -15,14 +15,16 @@
 //   warp 0  TMA producer: Q tile once, K tiles (128 keys) into a 3-4 stage ring
 //   warp 1  tcgen05 issuer: S = Q.K^T (M=128, N=128, K=d) into one of two TMEM
 //           buffers (fp32, 128 lanes x 128 columns each)
-//   statistics warps, one thread per query row (its TMEM lane): block max,
+//   statistics warps, one thread per query row (its TMEM lane): running max,
 //           lazily re-referenced exp2, per-(row, key-block) partial sums kept
-//           in TMEM columns 256..511 (so at most 256 key blocks per row),
-//           running row sum.  A reference value only moves when the block max
-//           exceeds it by more than 2^8; the warp's stored partials are then
-//           rescaled in TMEM.  At B = 64 two warps share each lane quadrant,
-//           one per 64-column block of the S tile, with separate references
-//           that are merged per row at the end (columns 256..383 / 384..511).
+//           in TMEM columns 256..511, running row sum.  A reference value
+//           only moves when a 32-column chunk's max exceeds it by more than
+//           2^8; the warp's stored partials are then rescaled in TMEM.  Each
+//           lane quadrant has two warps: at B = 64 one per 64-column block of
+//           every tile, at B = 128 one per S buffer (every second tile, in
+//           32-column chunks); each has its own reference and the parts are
+//           merged per row at the end.  128 partial columns per warp
+//           (sequences up to 16384 tokens at B = 64, 32768 at B = 128).
 //   end:    mass[bi][bj] = sum over the block-row's rows of partial/l_ref,
 //           reduced across lanes with a 31-shuffle transpose-reduction and
 //           across warps in a fixed order (deterministic).
@@ -106,11 +108,17 @@ __device__ __forceinline__ void rescale_parts(uint32_t taddr, int ncols, float a
   tc_wait_st();
 }
 
-// Statistics warps: at B = 64 two per TMEM lane quadrant (each owns one
-// 64-column block of every 128-column S tile); at B = 128 one per quadrant.
+// Statistics warps per TMEM lane quadrant: at B = 64 two, one per 64-column
+// block of every S tile (each loads its 64 columns at once and frees the
+// buffer); at B = 128 two, one per S buffer (each takes every second tile in
+// 32-column chunks, which keeps its registers in the file).
 template <int BLK>
 struct StatWarps {
-  static constexpr int kN = (BLK == 64) ? 8 : 4;
+  static constexpr int kHalves = (BLK == 64) ? 2 : 1;  // blocks per tile
+  static constexpr int kPar = (BLK == 64) ? 1 : 2;     // buffers split between warps
+  static constexpr int kParts = kHalves * kPar;
+  static constexpr int kCW = (BLK == 64) ? 64 : 32;    // columns per pass
+  static constexpr int kN = 4 * kParts;
   static constexpr int kThreads = 64 + 32 * kN;
 };
 
@@ -158,7 +166,7 @@ __global__ void __launch_bounds__(StatWarps<BLK>::kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(barSFull(b), 1);
-      mbar_init(barSEmpty(b), StatWarps<BLK>::kN);
+      mbar_init(barSEmpty(b), StatWarps<BLK>::kN / StatWarps<BLK>::kPar);  // the warps of that buffer
     }
     mbar_init(barDone, 1);
     *stat_fail = 0;
@@ -256,13 +264,19 @@ __global__ void __launch_bounds__(StatWarps<BLK>::kThreads, 1)
   } else {
     // ---------------------------------------------------------- statistics
     constexpr int kSW = StatWarps<BLK>::kN;
-    constexpr int kW = (BLK == 64) ? 64 : 128;  // S columns per warp per tile (one block)
+    constexpr int kParts = StatWarps<BLK>::kParts;
+    constexpr int kPar = StatWarps<BLK>::kPar;
+    constexpr int kCW = StatWarps<BLK>::kCW;
+    constexpr int kChunks = BLK / kCW;                // passes over this warp's block
     const int wq = warp & 3;
-    const int half = (BLK == 64) ? ((warp - 2) >> 2) : 0;
+    const int part = (warp - 2) >> 2;                 // 0 .. kParts-1
+    const int half = part % StatWarps<BLK>::kHalves;  // block of the tile
+    const int parity = part / StatWarps<BLK>::kHalves;  // S buffer (kPar = 2)
     const int row = wq * 32 + lane;
     const uint32_t trow = tmem + (static_cast<uint32_t>(wq * 32) << 16);
-    const uint32_t partcol = kPartCol + half * 128;  // this warp's per-block partials
+    const uint32_t partcol = kPartCol + part * (256 / kParts);  // this warp's per-block partials
     const float sc = p.scale_log2;
+    const float2 sc2 = make_float2(sc, sc);
     float* red = reinterpret_cast<float*>(smem + Lay::kRed);
     float* xs = reinterpret_cast<float*>(smem + Lay::kX);
     int st = 0;
@@ -274,105 +288,112 @@ __global__ void __launch_bounds__(StatWarps<BLK>::kThreads, 1)
       const int n_ct = p.causal ? tile.tl + 1 : (tile.L + kCols - 1) / kCols;
       const int row_local = tile.tl * kRows + row;
       const bool row_ok = row_local < tile.L;
+      const int n_first = (kPar == 1) ? 0 : ((parity - st) & 1);  // first tile of this warp
       float mtrue = -INFINITY, ref = -INFINITY, lsum = 0.f;
       int nblk = 0;
       bool ok = true;
-      for (int n = 0; n < n_ct; ++n, ++st) {
-        const int b = st & 1;
-        if (!warp_wait(barSFull(b), (st >> 1) & 1, p.err)) {
+      for (int n = n_first; n < n_ct; n += kPar) {
+        const int sn = st + n;
+        const int b = sn & 1;
+        if (!warp_wait(barSFull(b), (sn >> 1) & 1, p.err)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        float x[kW];
-        {
-          uint32_t* rr = reinterpret_cast<uint32_t*>(x);
+        float bs = 0.f;  // this block's partial, relative to the current reference
+#pragma unroll 1
+        for (int c = 0; c < kChunks; ++c) {
+          float x[kCW];
 #pragma unroll
-          for (int c = 0; c < kW; c += 32) tmem_ld32(trow + b * kCols + half * 64 + c, rr + c);
-        }
-        tc_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(barSEmpty(b));
-        const int col0 = n * kCols + half * 64;
-        if (n == n_ct - 1) {  // only the last tile can cross the diagonal or the sequence end
-#pragma unroll
-          for (int c = 0; c < kW; ++c) {
-            const int j = col0 + c;
-            if (!((j < tile.L) && (!p.causal || j <= row_local))) x[c] = -INFINITY;
+          for (int e = 0; e < kCW; e += 32)
+            tmem_ld32(trow + b * kCols + half * 64 + c * kCW + e, reinterpret_cast<uint32_t*>(x) + e);
+          tc_wait_ld();
+          if (c == kChunks - 1) {  // the whole block is in registers or consumed: free the buffer
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(barSEmpty(b));
           }
-        }
-        // block max on the raw scores (scaling by sc > 0 preserves order)
-        float m0 = -INFINITY, m1 = -INFINITY;
+          const int col0 = n * kCols + half * 64 + c * kCW;
+          if (n == n_ct - 1) {  // only the last tile can cross the diagonal or the sequence end
 #pragma unroll
-        for (int c = 0; c < kW; c += 4) {
-          m0 = fmax3(m0, x[c], x[c + 1]);
-          m1 = fmax3(m1, x[c + 2], x[c + 3]);
-        }
-        float bm = fmaxf(m0, m1) * sc;
-        if (!row_ok) bm = -INFINITY;
-        mtrue = fmaxf(mtrue, bm);
-        float alpha = 1.f;
-        if (bm > ref + kTau) {
-          alpha = (ref == -INFINITY) ? 0.f : ex2(ref - bm);
-          ref = bm;
-          lsum *= alpha;
-        }
-        if (__any_sync(0xffffffffu, alpha != 1.f) && nblk > 0) {
-          tc_wait_st();
-          rescale_parts(trow + partcol, nblk, alpha);
-        }
-        // exp2(x * sc - ref) with one packed FMA per two scores, packed sums
-        const float nrs = (ref == -INFINITY) ? 0.f : -ref;
-        const float2 sc2 = make_float2(sc, sc), nrs2 = make_float2(nrs, nrs);
-        float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+            for (int e = 0; e < kCW; ++e) {
+              const int j = col0 + e;
+              if (!((j < tile.L) && (!p.causal || j <= row_local))) x[e] = -INFINITY;
+            }
+          }
+          // chunk max on the raw scores (scaling by sc > 0 preserves order)
+          float m0 = -INFINITY, m1 = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < kW; c += 4) {
-          float2 t0 = ffma2(make_float2(x[c], x[c + 1]), sc2, nrs2);
-          float2 t1 = ffma2(make_float2(x[c + 2], x[c + 3]), sc2, nrs2);
-          t0.x = ex2(t0.x);
-          t0.y = ex2(t0.y);
-          t1.x = ex2(t1.x);
-          t1.y = ex2(t1.y);
-          acc0 = fadd2(acc0, t0);
-          acc1 = fadd2(acc1, t1);
+          for (int e = 0; e < kCW; e += 4) {
+            m0 = fmax3(m0, x[e], x[e + 1]);
+            m1 = fmax3(m1, x[e + 2], x[e + 3]);
+          }
+          float bm = fmaxf(m0, m1) * sc;
+          if (!row_ok) bm = -INFINITY;
+          mtrue = fmaxf(mtrue, bm);
+          float alpha = 1.f;
+          if (bm > ref + kTau) {
+            alpha = (ref == -INFINITY) ? 0.f : ex2(ref - bm);
+            ref = bm;
+            lsum *= alpha;
+            bs *= alpha;
+          }
+          if (__any_sync(0xffffffffu, alpha != 1.f) && nblk > 0) {
+            tc_wait_st();
+            rescale_parts(trow + partcol, nblk, alpha);
+          }
+          // exp2(x * sc - ref) with one packed FMA per two scores, packed sums
+          const float nrs = (ref == -INFINITY) ? 0.f : -ref;
+          const float2 nrs2 = make_float2(nrs, nrs);
+          float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int e = 0; e < kCW; e += 4) {
+            float2 t0 = ffma2(make_float2(x[e], x[e + 1]), sc2, nrs2);
+            float2 t1 = ffma2(make_float2(x[e + 2], x[e + 3]), sc2, nrs2);
+            t0.x = ex2(t0.x);
+            t0.y = ex2(t0.y);
+            t1.x = ex2(t1.x);
+            t1.y = ex2(t1.y);
+            acc0 = fadd2(acc0, t0);
+            acc1 = fadd2(acc1, t1);
+          }
+          bs += (acc0.x + acc0.y) + (acc1.x + acc1.y);
         }
-        float bs = (acc0.x + acc0.y) + (acc1.x + acc1.y);
         if (!row_ok) bs = 0.f;
         lsum += bs;
         tmem_st1(trow + partcol + nblk, __float_as_uint(bs));
         ++nblk;
       }
       tc_wait_st();
+      st += n_ct;
       // ------------------------------------------------------ item epilogue
       // A warp whose wait gave up flags it before the barrier; every warp
       // reads the flag after it, so all take the same exit.
       if (!ok && lane == 0) *stat_fail = 1;
-      if (BLK == 64) {
-        xs[(half * 3 + 0) * 128 + row] = mtrue;
-        xs[(half * 3 + 1) * 128 + row] = ref;
-        xs[(half * 3 + 2) * 128 + row] = lsum;
-      }
+      xs[(part * 3 + 0) * 128 + row] = mtrue;
+      xs[(part * 3 + 1) * 128 + row] = ref;
+      xs[(part * 3 + 2) * 128 + row] = lsum;
       named_bar(1, 32 * kSW);
       const bool good = (*stat_fail == 0);
-      float M = mtrue, Rf = ref, Lt = lsum, own_scale = 1.f;
-      if (BLK == 64) {
-        // merge the two column halves of each row (separate lazy references)
-        const int oh = half ^ 1;
-        const float mo = xs[(oh * 3 + 0) * 128 + row], ro = xs[(oh * 3 + 1) * 128 + row],
-                    lo = xs[(oh * 3 + 2) * 128 + row];
-        M = fmaxf(mtrue, mo);
-        Rf = fmaxf(ref, ro);
-        if (Rf == -INFINITY) {
-          Lt = 0.f;
-        } else {
-          own_scale = (ref == -INFINITY) ? 0.f : ex2(ref - Rf);
-          const float other = (ro == -INFINITY) ? 0.f : ex2(ro - Rf);
-          Lt = lsum * own_scale + lo * other;
+      // merge the parts of each row (separate lazy references), in part order
+      float M = -INFINITY, Rf = -INFINITY;
+#pragma unroll
+      for (int q = 0; q < kParts; ++q) {
+        M = fmaxf(M, xs[(q * 3 + 0) * 128 + row]);
+        Rf = fmaxf(Rf, xs[(q * 3 + 1) * 128 + row]);
+      }
+      float Lt = 0.f, own_scale = 0.f;
+      if (Rf != -INFINITY) {
+#pragma unroll
+        for (int q = 0; q < kParts; ++q) {
+          const float rq = xs[(q * 3 + 1) * 128 + row];
+          const float sq = (rq == -INFINITY) ? 0.f : ex2(rq - Rf);
+          Lt += xs[(q * 3 + 2) * 128 + row] * sq;
+          if (q == part) own_scale = sq;
         }
       }
       const float inv = (row_ok && Lt > 0.f) ? own_scale / Lt : 0.f;
-      if (good && row_ok && half == 0) {
+      if (good && row_ok && part == 0) {
         const size_t o = static_cast<size_t>(h) * p.T + tile.seq_start + row_local;
         p.row_max[o] = M * kLn2;
         p.row_sum[o] = Lt * ex2(Rf - M);
@@ -386,13 +407,14 @@ __global__ void __launch_bounds__(StatWarps<BLK>::kThreads, 1)
         for (int i = 0; i < 32; ++i) f[i] = (c0 + i < nblk) ? __uint_as_float(v[i]) * inv : 0.f;
         const float tot = transpose_reduce32(f);
         const int k = c0 + lane;
-        if (k < nblk) red[wq * 256 + (BLK == 64 ? 2 * k + half : k)] = tot;
+        const int n = n_first + kPar * k;  // tile of this warp's k-th partial
+        if (k < nblk) red[wq * 256 + (BLK == 64 ? 2 * n + half : n)] = tot;
       }
       tc_fence_before();
       named_bar(1, 32 * kSW);
       if (!good) break;
       const int t0 = threadIdx.x - 64;
-      const int nbt = (BLK == 64) ? 2 * nblk : nblk;  // block columns covered
+      const int nbt = (BLK == 64) ? 2 * n_ct : n_ct;  // block columns covered
       if (BLK == 64) {
         for (int t = t0; t < 2 * nbt; t += 32 * kSW) {
           const int hb = t / nbt, c = t - hb * nbt;
