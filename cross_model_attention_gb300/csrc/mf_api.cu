@@ -113,7 +113,7 @@ struct ProfRec {
 
 struct mf_bsr_s {
   bool exact_alloc = false;  // size the BSR exactly (one stream sync per layer)
-  bool profiling = false;
+  unsigned prof_mask = 0;  // kernel kinds timed with events
   long long launches[MF_K_COUNT] = {0};
   std::vector<ProfRec> prof;
   std::vector<cudaEvent_t> event_pool;
@@ -186,7 +186,7 @@ cudaEvent_t take_event(mf_bsr_t h) {
 template <typename F>
 cudaError_t timed(mf_bsr_t h, int kind, cudaStream_t s, F&& launch) {
   h->launches[kind] += 1;
-  if (!h->profiling) return launch();
+  if (!((h->prof_mask >> kind) & 1u)) return launch();
   cudaEvent_t a = take_event(h), b = take_event(h);
   if (a) cudaEventRecord(a, s);
   cudaError_t e = launch();
@@ -678,9 +678,10 @@ int mf_device_status(mf_bsr_t h, void* stream) {
   return MF_OK;
 }
 
-int mf_profile(mf_bsr_t h, int enable) {
+int mf_profile_kinds(mf_bsr_t h, int mask) {
   if (!h) return fail(MF_ERR_ARG, "handle is NULL");
-  if (enable) {
+  const unsigned m = static_cast<unsigned>(mask) & ((1u << MF_K_COUNT) - 1u);
+  if (m) {
     for (auto& r : h->prof) {
       h->event_pool.push_back(r.a);
       h->event_pool.push_back(r.b);
@@ -688,8 +689,12 @@ int mf_profile(mf_bsr_t h, int enable) {
     h->prof.clear();
     for (auto& c : h->launches) c = 0;
   }
-  h->profiling = enable != 0;
+  h->prof_mask = m;
   return MF_OK;
+}
+
+int mf_profile(mf_bsr_t h, int enable) {
+  return mf_profile_kinds(h, enable ? static_cast<int>((1u << MF_K_COUNT) - 1u) : 0);
 }
 
 int mf_profile_read(mf_bsr_t h, int kernel, int64_t* launches, double* total_ms) {

@@ -22,7 +22,7 @@ MF_DTYPE_F32, MF_DTYPE_BF16 = 0, 1
 EXPORTED = ("mf_version", "mf_last_error", "mf_supported", "mf_bsr_create", "mf_bsr_destroy",
             "mf_compress", "mf_retrieve", "mf_bsr_info", "mf_bsr_export", "mf_bsr_copy",
             "mf_bsr_release_layer", "mf_device_status", "mf_selftest_wait", "mf_profile",
-            "mf_profile_read", "mf_select_noalloc", "mf_bsr_set_exact")
+            "mf_profile_read", "mf_profile_kinds", "mf_select_noalloc", "mf_bsr_set_exact")
 KERNELS = ("stats", "select", "scan", "pack", "union", "retrieve")
 
 
@@ -69,6 +69,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mf_select_noalloc.argtypes = [vp, ctypes.POINTER(ctypes.c_int32), i32, i32, i32, i32,
                                       ctypes.c_float, vp, vp, ctypes.c_int64, vp, vp]
     lib.mf_profile.argtypes = [vp, i32]
+    lib.mf_profile_kinds.argtypes = [vp, i32]
     lib.mf_profile_read.argtypes = [vp, i32, i64p, ctypes.POINTER(ctypes.c_double)]
     for name in EXPORTED:
         getattr(lib, name)
@@ -204,6 +205,10 @@ def mf_profile(h, enable: bool) -> None:
     _check(load_library().mf_profile(h, int(enable)))
 
 
+def mf_profile_kinds(h, mask: int) -> None:
+    _check(load_library().mf_profile_kinds(h, int(mask)))
+
+
 def mf_profile_read(h, kernel: int):
     n, ms = ctypes.c_int64(), ctypes.c_double()
     _check(load_library().mf_profile_read(h, kernel, ctypes.byref(n), ctypes.byref(ms)))
@@ -266,6 +271,10 @@ class BSR:
 
     def profile(self, enable: bool) -> None:
         mf_profile(self.handle, enable)
+
+    def profile_kinds(self, names) -> None:
+        """Time only the named kernel kinds (e.g. ("stats", "pack"))."""
+        mf_profile_kinds(self.handle, sum(1 << KERNELS.index(n) for n in names))
 
     def profile_read(self) -> Dict[str, tuple]:
         """{kernel: (launches, total device ms)} since profiling was enabled."""

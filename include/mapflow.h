@@ -248,6 +248,13 @@ MF_API int mf_device_status(mf_bsr_t h, void* stream);
 MF_API int mf_profile(mf_bsr_t h, int enable);
 
 /*
+ * mf_profile_kinds — like mf_profile, but times only the kernel kinds whose
+ * bit (1 << MF_K_*) is set in `mask` (0 disables timing).  Fewer event pairs
+ * in the stream: launch counts stay complete for every kind.
+ */
+MF_API int mf_profile_kinds(mf_bsr_t h, int mask);
+
+/*
  * mf_profile_read — launches and summed device time (ms) of one kernel kind
  * since profiling was enabled.  Waits for the recorded events.
  */
