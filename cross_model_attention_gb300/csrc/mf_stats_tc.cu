@@ -321,14 +321,17 @@ __global__ void __launch_bounds__(StatWarps<BLK>::kThreads, 1)
               if (!((j < tile.L) && (!p.causal || j <= row_local))) x[e] = -INFINITY;
             }
           }
-          // chunk max on the raw scores (scaling by sc > 0 preserves order)
-          float m0 = -INFINITY, m1 = -INFINITY;
+          // chunk max on the raw scores (scaling by sc > 0 preserves order),
+          // four independent chains
+          float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
 #pragma unroll
-          for (int e = 0; e < kCW; e += 4) {
+          for (int e = 0; e < kCW; e += 8) {
             m0 = fmax3(m0, x[e], x[e + 1]);
             m1 = fmax3(m1, x[e + 2], x[e + 3]);
+            m2 = fmax3(m2, x[e + 4], x[e + 5]);
+            m3 = fmax3(m3, x[e + 6], x[e + 7]);
           }
-          float bm = fmaxf(m0, m1) * sc;
+          float bm = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3)) * sc;
           if (!row_ok) bm = -INFINITY;
           mtrue = fmaxf(mtrue, bm);
           float alpha = 1.f;
@@ -345,19 +348,31 @@ __global__ void __launch_bounds__(StatWarps<BLK>::kThreads, 1)
           // exp2(x * sc - ref) with one packed FMA per two scores, packed sums
           const float nrs = (ref == -INFINITY) ? 0.f : -ref;
           const float2 nrs2 = make_float2(nrs, nrs);
+          // four independent packed accumulators
           float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+          float2 acc2 = make_float2(0.f, 0.f), acc3 = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int e = 0; e < kCW; e += 4) {
+          for (int e = 0; e < kCW; e += 8) {
             float2 t0 = ffma2(make_float2(x[e], x[e + 1]), sc2, nrs2);
             float2 t1 = ffma2(make_float2(x[e + 2], x[e + 3]), sc2, nrs2);
+            float2 t2 = ffma2(make_float2(x[e + 4], x[e + 5]), sc2, nrs2);
+            float2 t3 = ffma2(make_float2(x[e + 6], x[e + 7]), sc2, nrs2);
             t0.x = ex2(t0.x);
             t0.y = ex2(t0.y);
             t1.x = ex2(t1.x);
             t1.y = ex2(t1.y);
+            t2.x = ex2(t2.x);
+            t2.y = ex2(t2.y);
+            t3.x = ex2(t3.x);
+            t3.y = ex2(t3.y);
             acc0 = fadd2(acc0, t0);
             acc1 = fadd2(acc1, t1);
+            acc2 = fadd2(acc2, t2);
+            acc3 = fadd2(acc3, t3);
           }
-          bs += (acc0.x + acc0.y) + (acc1.x + acc1.y);
+          const float2 a01 = fadd2(acc0, acc1), a23 = fadd2(acc2, acc3);
+          const float2 a = fadd2(a01, a23);
+          bs += a.x + a.y;
         }
         if (!row_ok) bs = 0.f;
         lsum += bs;
