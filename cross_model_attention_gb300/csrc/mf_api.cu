@@ -137,6 +137,10 @@ struct mf_bsr_s {
   void* ring = nullptr;
   uint32_t* ring_flags = nullptr;
   int ring_teams = 0;
+  // team retrieval's slab lists (longest-first onto the least-loaded team)
+  std::vector<int> team_slabs;
+  int* team_slabs_d = nullptr;
+  int team_slab_teams = 0, team_stride = 0;
 };
 
 namespace {
@@ -330,6 +334,7 @@ void mf_bsr_destroy(mf_bsr_t h) {
   dev_free(h, h->err_d, nullptr);
   dev_free(h, h->ring, nullptr);
   dev_free(h, h->ring_flags, nullptr);
+  dev_free(h, h->team_slabs_d, nullptr);
   cudaDeviceSynchronize();
   if (h->host_pinned) cudaFreeHost(h->host_pinned);
   delete h;
@@ -551,6 +556,36 @@ int mf_retrieve(mf_bsr_t h, const float* W, const void* v, void* o, int dtype, i
           if (!h->ring || !h->ring_flags) return fail(MF_ERR_OOM, "exchange ring allocation failed");
           h->ring_teams = cap;
         }
+        if (h->team_slab_teams != teams) {
+          // Work of a slab ~ its candidate blocks (causal: bi + 1); slabs come
+          // heaviest first, each goes to the team with the least work so far.
+          std::vector<std::vector<int>> lists(teams);
+          std::vector<long long> load(teams, 0);
+          for (int i = 0; i < h->n_slabs; ++i) {
+            const RowBlock& rb = h->rbs[h->slabs[i].rb];
+            const long long wgt = h->causal ? rb.bi + 1 : (rb.L + h->B - 1) / h->B;
+            int best = 0;
+            for (int t = 1; t < teams; ++t)
+              if (load[t] < load[best]) best = t;
+            lists[best].push_back(i);
+            load[best] += wgt;
+          }
+          int stride = 1;
+          for (auto& l : lists) stride = std::max(stride, (int)l.size());
+          h->team_slabs.assign((size_t)teams * stride, -1);
+          for (int t = 0; t < teams; ++t)
+            for (size_t j = 0; j < lists[t].size(); ++j) h->team_slabs[(size_t)t * stride + j] = lists[t][j];
+          dev_free(h, h->team_slabs_d, s);
+          h->team_slabs_d = (int*)dev_alloc(h, h->team_slabs.size() * sizeof(int), s);
+          if (!h->team_slabs_d) return fail(MF_ERR_OOM, "slab table allocation failed");
+          MF_CUDA(cudaMemcpyAsync(h->team_slabs_d, h->team_slabs.data(), h->team_slabs.size() * sizeof(int),
+                                  cudaMemcpyHostToDevice, s),
+                  "slab table copy");
+          h->team_slab_teams = teams;
+          h->team_stride = stride;
+        }
+        rp.team_slabs = h->team_slabs_d;
+        rp.team_stride = h->team_stride;
         CUtensorMap ta{};
         rc = make_map(&ta, h->ring, 64, (uint64_t)retrieve_team_ring_rows(h->ring_teams), 128, 64,
                       (uint32_t)retrieve_team_ring_box_rows(H_r));

@@ -65,6 +65,8 @@ struct RetrieveParams {
   const int* union_cnt;   // [R]
   const int* union_list;  // [C]
   const int* utile;       // [C][H_s] tile_of in union order
+  const int* team_slabs;  // team retrieval: [n_teams][team_stride] slab indices, -1 padded
+  int team_stride;
   const float* W;         // [H_r][H_s] of this receiver layer
   int zero_tile;          // index of an all-zero tile (= nnz)
   const uint16_t* values; // [nnz+1][B][B] bf16 tiles

@@ -35,7 +35,8 @@
 //     slab's blocks, then bumps the slot's freed counter.
 // The ring (6 slots per team) lives in L2 between its write and its reads;
 // every sender-tile byte is read from HBM once.  Slabs go to teams heaviest
-// first in a snake order; within a team all CTAs walk the same slab list,
+// first onto the least-loaded team (a host-side table); within a team all
+// CTAs walk the same slab list,
 // whose records are staged in shared memory at the start.
 //
 // Warp roles (512 threads): warp 0 TMA loads of V and of the group's A_hat^T,
@@ -119,17 +120,16 @@ __device__ __forceinline__ bool warp_wait_counter(const uint32_t* ptr, uint32_t 
   return ok != 0;
 }
 
-// Slab of round r for a team, in a snake order over the heavy-first slab
-// list; -1 once the list is exhausted.
-__device__ __forceinline__ int slab_of(int r, int team, int n_teams, int n_slabs) {
-  const int idx = r * n_teams + ((r & 1) ? (n_teams - 1 - team) : team);
-  return idx < n_slabs ? idx : -1;
+// Slab of round r for a team (the host's longest-first assignment); -1 once
+// the team's list is exhausted.
+__device__ __forceinline__ int slab_of(int r, int team, const RetrieveParams& p) {
+  return r < p.team_stride ? p.team_slabs[team * p.team_stride + r] : -1;
 }
 
 template <int kSub>
-__device__ __forceinline__ SlabRec load_slab(int r, const RetrieveParams& p, int team, int n_teams) {
+__device__ __forceinline__ SlabRec load_slab(int r, const RetrieveParams& p, int team) {
   SlabRec x{};
-  const int si = slab_of(r, team, n_teams, p.n_slabs);
+  const int si = slab_of(r, team, p);
   if (si < 0) {
     x.n_sub = -1;
     return x;
@@ -149,9 +149,9 @@ __device__ __forceinline__ SlabRec load_slab(int r, const RetrieveParams& p, int
 // Record r of the team's slab list (n_sub < 0 past the end).
 template <int kSub>
 __device__ __forceinline__ SlabRec slab_rec(int r, const SlabRec* tab, const RetrieveParams& p,
-                                            int team, int n_teams) {
+                                            int team) {
   if (r < kMaxSlabs) return tab[r];
-  return load_slab<kSub>(r, p, team, n_teams);
+  return load_slab<kSub>(r, p, team);
 }
 
 // Walks a team's blocks in order: slab after slab, kept block column after
@@ -163,10 +163,10 @@ struct BlockCursor {
 };
 template <int kSub>
 __device__ __forceinline__ void cursor_settle(BlockCursor& c, const SlabRec* tab,
-                                              const RetrieveParams& p, int team, int n_teams) {
+                                              const RetrieveParams& p, int team) {
   while (c.r < 0 || c.j >= c.s.n_sub) {
     ++c.r;
-    c.s = slab_rec<kSub>(c.r, tab, p, team, n_teams);
+    c.s = slab_rec<kSub>(c.r, tab, p, team);
     if (c.s.n_sub < 0) {
       c.done = true;
       return;
@@ -187,7 +187,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sb = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int team = blockIdx.x / kTeam, g = blockIdx.x % kTeam;
-  const int n_teams = gridDim.x / kTeam;
   const int hpc = p.H_r / kTeam;
   const TeamLayout lay(D, p.H_s, hpc);
   constexpr int kSub = BLK / 64;
@@ -225,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int i = threadIdx.x; i < kPBytes / 16; i += kThreads)
     *reinterpret_cast<uint4*>(smem + lay.off_p + i * 16) = make_uint4(0u, 0u, 0u, 0u);
   // the team's slab records
-  for (int r = threadIdx.x; r < kMaxSlabs; r += kThreads) tab[r] = load_slab<kSub>(r, p, team, n_teams);
+  for (int r = threadIdx.x; r < kMaxSlabs; r += kThreads) tab[r] = load_slab<kSub>(r, p, team);
   // W^T as the combine's B operand: row n = 4 * group + head slot (32 rows;
   // receiver head group * H_r/8 + slot), 64 bf16 sender-head entries per row,
   // 128-byte swizzle; zero for unused slots and beyond H_s.
@@ -252,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       int u = 0;
       for (int r = 0; ok; ++r) {
-        const SlabRec sr = slab_rec<kSub>(r, tab, p, team, n_teams);
+        const SlabRec sr = slab_rec<kSub>(r, tab, p, team);
         if (sr.n_sub < 0) break;
         int bj_next = sr.n_sub > 0 ? p.union_list[sr.cand_off] : 0;
         for (int j = 0; j < sr.n_sub; ++j, ++u) {
@@ -305,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // arrivals on the previous blocks' slices).
     const int* idx_ring = reinterpret_cast<const int*>(smem + lay.off_i);
     BlockCursor ic;
-    cursor_settle<kSub>(ic, tab, p, team, n_teams);
+    cursor_settle<kSub>(ic, tab, p, team);
     int n_req = 0;
     auto request_next = [&]() {
       if (ic.done) return;
@@ -316,13 +315,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       cp_async_arrive(bar(kBarIdx + slot));
       ++n_req;
       ++ic.j;
-      cursor_settle<kSub>(ic, tab, p, team, n_teams);
+      cursor_settle<kSub>(ic, tab, p, team);
     };
     for (int i = 0; i < kIdxAhead; ++i) request_next();
     bool ok = true;
     int u = 0;
     for (int r = 0; ok; ++r) {
-      const SlabRec sr = slab_rec<kSub>(r, tab, p, team, n_teams);
+      const SlabRec sr = slab_rec<kSub>(r, tab, p, team);
       if (sr.n_sub < 0) break;
       for (int j = 0; ok && j < sr.n_sub; ++j, ++u) {
         const int cs = j % kSub;
@@ -371,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       int u = 0;
       for (int r = 0; ok; ++r) {
-        const SlabRec sr = slab_rec<kSub>(r, tab, p, team, n_teams);
+        const SlabRec sr = slab_rec<kSub>(r, tab, p, team);
         if (sr.n_sub < 0) break;
         for (int j = 0; ok && j < sr.n_sub; ++j, ++u) {
           const int b = u & 1, pb = u % lay.npb;
@@ -406,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       int u = 0;
       for (int r = 0; ok; ++r) {
-        const SlabRec sr = slab_rec<kSub>(r, tab, p, team, n_teams);
+        const SlabRec sr = slab_rec<kSub>(r, tab, p, team);
         if (sr.n_sub < 0) break;
         // the previous slab's output has been read out of TMEM
         if (r > 0 && !mbar_wait(bar(kBarOFree), (r - 1) & 1, p.err)) {
@@ -458,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int total = 0;
       for (int r = 0;; ++r) {
-        const SlabRec sr = slab_rec<kSub>(r, tab, p, team, n_teams);
+        const SlabRec sr = slab_rec<kSub>(r, tab, p, team);
         if (sr.n_sub < 0) break;
         total += sr.n_sub;
       }
@@ -489,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     int u = 0;
     for (int r = 0; ok; ++r) {
-      const SlabRec sr = slab_rec<kSub>(r, tab, p, team, n_teams);
+      const SlabRec sr = slab_rec<kSub>(r, tab, p, team);
       if (sr.n_sub < 0) break;
       const int row0 = sr.bi * BLK + sr.half * 64;
       for (int j = 0; ok && j < sr.n_sub; ++j, ++u) {
