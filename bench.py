@@ -243,6 +243,24 @@ def run_reference(args, rank: int, world: int):
     print(json.dumps(out), flush=True)
 
 
+def job_times(local_times, world: int, device):
+    """Per-quantity maximum over the ranks: the slowest replica sets the job
+    time (each rank runs the whole workload on its own GPU; no data path
+    between ranks)."""
+    import torch
+    t = torch.tensor(list(local_times), dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_throughput(units_per_rank: float, world: int, seconds: float) -> float:
+    """Whole-job throughput of `world` replicas that each processed
+    `units_per_rank` in the job time `seconds` (weak scaling)."""
+    return units_per_rank * world / seconds
+
+
 def config_dict(w, rcv, world):
     return {"workload": f"workload {w.index}: {w.name}", "sender_layers": w.sender_layers,
             "sender_heads": w.sender_heads, "sender_kv_heads": w.sender_kv_heads,
@@ -329,13 +347,10 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
     t_comp = sum(e[0].elapsed_time(e[1]) for e in evs) / 1e3
     t_ret = sum(e[1].elapsed_time(e[2]) for e in evs) / 1e3
     t_step = evs[0][0].elapsed_time(evs[-1][2]) / 1e3
-    times = torch.tensor([t_step, t_comp, t_ret], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    t_step, t_comp, t_ret = times.tolist()
+    t_step, t_comp, t_ret = job_times([t_step, t_comp, t_ret], world, dev)
     K = args.steps
-    value = ret_bytes * K * world / t_ret / 1e9
-    comp_tps = T * Ls * K * world / t_comp
+    value = job_throughput(ret_bytes * K, world, t_ret) / 1e9
+    comp_tps = job_throughput(T * Ls * K, world, t_comp)
 
     peaks, src = load_peaks()
     hbm = float(peaks["hbm_gbs"])
