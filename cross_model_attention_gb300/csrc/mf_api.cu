@@ -118,7 +118,7 @@ struct mf_bsr_s {
   std::vector<ProfRec> prof;
   std::vector<cudaEvent_t> event_pool;
   int n_layers = 0, T = 0, H_s = 0, B = 0, causal = 1, n_seqs = 0;
-  int R = 0, C = 0, n_tiles = 0, n_slabs = 0;
+  int R = 0, C = 0, max_cand = 0, n_tiles = 0, n_slabs = 0;
   std::vector<int> cu;
   std::vector<RowBlock> rbs;
   std::vector<RowTile> tiles;
@@ -258,6 +258,7 @@ int mf_bsr_create(mf_bsr_t* out, int n_layers, int T, int H_s, int B, int causal
     for (int bi = 0; bi < nb; ++bi) {
       h->rbs.push_back(RowBlock{start, L, bi, (int)cand});
       cand += causal ? bi + 1 : nb;
+      h->max_cand = std::max(h->max_cand, causal ? bi + 1 : nb);
       for (int half = 0; half < B / 64; ++half)
         if (bi * B + half * 64 < L) h->slabs.push_back(RowSlab{rb_first + bi, half});
     }
@@ -397,6 +398,7 @@ int mf_compress(mf_bsr_t h, int layer, const void* q, const void* k, int dtype, 
   cp.causal = causal;
   cp.R = h->R;
   cp.C = h->C;
+  cp.max_cand = h->max_cand;
   cp.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d));
   cp.p = p;
   cp.mass = L.mass;

@@ -37,6 +37,7 @@ struct CompressParams {
   int T, H_s, H_ks, d, B, causal;
   int R;            // block-rows
   int C;            // candidates per head
+  int max_cand;     // most candidates of one block-row
   float scale_log2; // log2(e) / sqrt(d)
   float p;
   // outputs / intermediates

@@ -32,8 +32,8 @@ struct PackLayout {
   static constexpr int kQBytes = kRows * D * 2;
   static constexpr int kKChunk = BLK * 128;            // BLK key rows x 64 bf16
   static constexpr int kKBytes = BLK * D * 2;
-  static constexpr int kStages = 2;  // keeps two CTAs per SM at B = 64
-  static constexpr int kStageBytes = 2 * ((BLK == 64) ? 2 * 64 * 128 : 2 * 128 * 128);  // 2 staging buffers
+  static constexpr int kStages = 3;  // with one staging buffer: still two CTAs per SM at B = 64
+  static constexpr int kStageBytes = (BLK == 64) ? 2 * 64 * 128 : 2 * 128 * 128;  // one staging buffer
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + kQBytes;
   static constexpr int kStg = kK + kStages * kKBytes;
@@ -243,7 +243,7 @@ __global__ void __launch_bounds__(kPackThreads, (BLK == 64) ? 2 : 1)
     //          BLK=128 -> per buffer one 32 KB tile as two 64-column boxes
     const uint32_t stg = sb + Lay::kStg;
     uint8_t* stg_g = smem + Lay::kStg;
-    constexpr int kBuf = Lay::kStageBytes / 2;
+    constexpr int kBuf = Lay::kStageBytes;
     const int grp_threads = (BLK == 64) ? 128 : 256;
     const int bar_id = (BLK == 64) ? 2 + sub : 2;
     const bool leader = ((BLK == 64) ? (rloc == 0) : (row == 0)) && ch == 0;
@@ -266,11 +266,11 @@ __global__ void __launch_bounds__(kPackThreads, (BLK == 64) ? 2 : 1)
       const int pos = (sub == 0) ? u_pos0[u] : u_pos1[u];
       if (pos < 0) continue;  // this block-row does not keep the block (group-uniform)
       const int bj = u_bj[u];
-      const int sbuf = nstore & 1;
+      const int sbuf = 0;
       ++nstore;
-      // the store issued from this staging buffer two tiles ago must have
-      // finished reading it
-      if (leader) bulk_wait_read_1();
+      // the store issued from the staging buffer one tile ago must have
+      // finished reading it (one buffer leaves room for a third K stage)
+      if (leader) bulk_wait_read_0();
       named_bar(bar_id, grp_threads);
       // only the diagonal block and the sequence's last block need masking
       const bool edge = !row_ok || (bj * BLK + BLK > tile.L) ||

@@ -13,8 +13,9 @@
 // (Every mass is <= B <= 128, so Tot < 2^40 and both sides stay below 2^60.)
 //
 // Kernels here:
-//   select_kernel   one CTA per BSR row: bitonic sort of the candidates in
-//                   shared memory, fixed-point prefix sum, kept list ascending
+//   select_kernel   one warp per BSR row: bitonic sort of the candidates in
+//                   registers, fixed-point prefix sum by warp shuffles, kept
+//                   list ascending by ballots
 //   scan_kernel     row_ptr = exclusive scan of the kept counts (single CTA,
 //                   warp-aggregated: per-thread serial chunk, warp shuffles,
 //                   one shared-memory pass over warp totals)
@@ -30,91 +31,125 @@ namespace {
 constexpr int kSelThreads = 256;
 constexpr int kMaxCand = 512;  // >= 256 blocks per row (non-causal worst case)
 
+// 64-bit shuffle (two 32-bit halves).
+__device__ __forceinline__ unsigned long long shfl_xor64(unsigned long long v, int m) {
+  const uint32_t lo = __shfl_xor_sync(0xffffffffu, static_cast<uint32_t>(v), m);
+  const uint32_t hi = __shfl_xor_sync(0xffffffffu, static_cast<uint32_t>(v >> 32), m);
+  return (static_cast<unsigned long long>(hi) << 32) | lo;
+}
+__device__ __forceinline__ unsigned long long shfl_up64(unsigned long long v, int d) {
+  const uint32_t lo = __shfl_up_sync(0xffffffffu, static_cast<uint32_t>(v), d);
+  const uint32_t hi = __shfl_up_sync(0xffffffffu, static_cast<uint32_t>(v >> 32), d);
+  return (static_cast<unsigned long long>(hi) << 32) | lo;
+}
+
+// One warp per BSR row (h, block-row); a CTA of 8 warps takes 8 rows.  The
+// row's candidates (at most 32 * E) are held E per lane, element i = lane*E +
+// e: 64-bit keys (inverted mass bits, column) are bitonic-sorted ascending in
+// registers (shuffles across lanes, compare-exchange within a lane), then the
+// fixed-point values in sorted order are prefix-summed with warp shuffles and
+// the kept columns are compacted in ascending order with ballots.
+template <int E>
 __global__ void __launch_bounds__(kSelThreads) select_kernel(const CompressParams p) {
-  __shared__ unsigned long long key[kMaxCand];
-  __shared__ unsigned long long pre[kMaxCand];
-  __shared__ int flag[kMaxCand];
-  const int row = blockIdx.x;            // h * R + rb
+  constexpr int N = 32 * E;
+  __shared__ int flag_s[kSelThreads / 32][N];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * (kSelThreads / 32) + warp;  // h * R + rb
+  if (row >= p.H_s * p.R) return;  // warp-uniform; no CTA-wide barrier below
   const int h = row / p.R, rb = row - h * p.R;
   const RowBlock rbk = p.rbs[rb];
   const int nb = (rbk.L + p.B - 1) / p.B;
   const int n = p.causal ? rbk.bi + 1 : nb;
-  int npow = 1;
-  while (npow < n) npow <<= 1;
   const float* mass = p.mass + static_cast<size_t>(h) * p.C + rbk.cand_off;
+  int* flag = flag_s[warp];
 
-  for (int i = threadIdx.x; i < npow; i += blockDim.x) {
+  unsigned long long key[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int i = lane * E + e;
     if (i < n) {
       const uint32_t bits = __float_as_uint(mass[i]);  // masses are >= 0
-      key[i] = (static_cast<unsigned long long>(0xFFFFFFFFu - bits) << 32) | static_cast<uint32_t>(i);
+      key[e] = (static_cast<unsigned long long>(0xFFFFFFFFu - bits) << 32) | static_cast<uint32_t>(i);
     } else {
-      key[i] = ~0ull;
+      key[e] = ~0ull;
     }
-    flag[i] = 0;
   }
-  __syncthreads();
+  for (int c = lane; c < N; c += 32) flag[c] = 0;
   // bitonic sort, ascending key == mass descending, column ascending
-  for (int k = 2; k <= npow; k <<= 1) {
+#pragma unroll
+  for (int k = 2; k <= N; k <<= 1) {
+#pragma unroll
     for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int i = threadIdx.x; i < npow; i += blockDim.x) {
-        const int ixj = i ^ j;
-        if (ixj > i) {
-          const unsigned long long a = key[i], b = key[ixj];
+      if (j >= E) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const int i = lane * E + e;
+          const unsigned long long other = shfl_xor64(key[e], j / E);
+          const bool up = (i & k) == 0, lower = (i & j) == 0;
+          key[e] = (lower == up) ? (key[e] < other ? key[e] : other)
+                                 : (key[e] < other ? other : key[e]);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          if (e & j) continue;
+          const int i = lane * E + e;
           const bool up = (i & k) == 0;
+          const unsigned long long a = key[e], b = key[e | j];
           if ((a > b) == up) {
-            key[i] = b;
-            key[ixj] = a;
+            key[e] = b;
+            key[e | j] = a;
           }
         }
       }
-      __syncthreads();
     }
   }
-  // fixed-point values in sorted order and their inclusive prefix sum
-  for (int i = threadIdx.x; i < npow; i += blockDim.x) {
+  // fixed-point values in sorted order; inclusive prefix within the lane,
+  // exclusive prefix of the lane totals across the warp
+  unsigned long long incl[E];
+  unsigned long long run = 0;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
     unsigned long long q = 0;
-    if (i < n) {
-      const int bj = static_cast<int>(key[i] & 0xFFFFFFFFu);
+    if (key[e] != ~0ull) {
+      const int bj = static_cast<int>(key[e] & 0xFFFFFFFFu);
       q = __double2ull_rn(static_cast<double>(mass[bj]) * 4294967296.0);
     }
-    pre[i] = q;
+    run += q;
+    incl[e] = run;
   }
-  __syncthreads();
-  for (int off = 1; off < npow; off <<= 1) {
-    unsigned long long add[kMaxCand / kSelThreads];
-    int c = 0;
-    for (int i = threadIdx.x; i < npow; i += blockDim.x, ++c) add[c] = (i >= off) ? pre[i - off] : 0ull;
-    __syncthreads();
-    c = 0;
-    for (int i = threadIdx.x; i < npow; i += blockDim.x, ++c) pre[i] += add[c];
-    __syncthreads();
+  unsigned long long scan = run;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const unsigned long long y = shfl_up64(scan, d);
+    if (lane >= d) scan += y;
   }
-  const unsigned long long tot = (n > 0) ? pre[n - 1] : 0ull;
+  const unsigned long long lane_base = scan - run;  // exclusive over lanes
+  const uint32_t tot_lo = __shfl_sync(0xffffffffu, static_cast<uint32_t>(scan), 31);
+  const uint32_t tot_hi = __shfl_sync(0xffffffffu, static_cast<uint32_t>(scan >> 32), 31);
+  const unsigned long long tot = (static_cast<unsigned long long>(tot_hi) << 32) | tot_lo;
   const unsigned long long thr = static_cast<unsigned long long>(
       __double2ull_rn(static_cast<double>(p.p) * 1048576.0)) * tot;
+  __syncwarp();
   // position i is kept iff its exclusive prefix is still below the threshold
-  for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    const unsigned long long excl = (i == 0) ? 0ull : pre[i - 1];
-    if ((excl << 20) < thr) flag[static_cast<int>(key[i] & 0xFFFFFFFFu)] = 1;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    if (key[e] == ~0ull) continue;
+    const unsigned long long excl = lane_base + (e == 0 ? 0ull : incl[e - 1]);
+    if ((excl << 20) < thr) flag[static_cast<int>(key[e] & 0xFFFFFFFFu)] = 1;
   }
-  __syncthreads();
-  // compact kept columns in ascending order (n <= 512: one thread per pair)
-  __shared__ int pos[kMaxCand];
-  for (int i = threadIdx.x; i < npow; i += blockDim.x) pos[i] = (i < n) ? flag[i] : 0;
-  __syncthreads();
-  for (int off = 1; off < npow; off <<= 1) {
-    int add[kMaxCand / kSelThreads];
-    int c = 0;
-    for (int i = threadIdx.x; i < npow; i += blockDim.x, ++c) add[c] = (i >= off) ? pos[i - off] : 0;
-    __syncthreads();
-    c = 0;
-    for (int i = threadIdx.x; i < npow; i += blockDim.x, ++c) pos[i] += add[c];
-    __syncthreads();
-  }
+  __syncwarp();
+  // compact the kept columns in ascending order
   int* out = p.keptcols + static_cast<size_t>(h) * p.C + rbk.cand_off;
-  for (int i = threadIdx.x; i < n; i += blockDim.x)
-    if (flag[i]) out[pos[i] - 1] = i;
-  if (threadIdx.x == 0) p.kcount[row] = (n > 0) ? pos[n - 1] : 0;
+  int cnt = 0;
+  for (int c0 = 0; c0 < n; c0 += 32) {
+    const int bj = c0 + lane;
+    const bool f = (bj < n) && flag[bj];
+    const uint32_t m = __ballot_sync(0xffffffffu, f);
+    if (f) out[cnt + __popc(m & ((1u << lane) - 1u))] = bj;
+    cnt += __popc(m);
+  }
+  if (lane == 0) p.kcount[row] = cnt;
 }
 
 constexpr int kScanThreads = 1024;
@@ -232,7 +267,13 @@ cudaError_t launch_selftest_wait(int* err, unsigned long long limit_ns, cudaStre
 }
 
 cudaError_t launch_select(const CompressParams& p, cudaStream_t s) {
-  select_kernel<<<p.H_s * p.R, kSelThreads, 0, s>>>(p);
+  const int rows = p.H_s * p.R;
+  const dim3 grid((rows + kSelThreads / 32 - 1) / (kSelThreads / 32));
+  if (p.max_cand <= 32) select_kernel<1><<<grid, kSelThreads, 0, s>>>(p);
+  else if (p.max_cand <= 64) select_kernel<2><<<grid, kSelThreads, 0, s>>>(p);
+  else if (p.max_cand <= 128) select_kernel<4><<<grid, kSelThreads, 0, s>>>(p);
+  else if (p.max_cand <= 256) select_kernel<8><<<grid, kSelThreads, 0, s>>>(p);
+  else return cudaErrorInvalidValue;  // at most 256 blocks per sequence
   return cudaGetLastError();
 }
 
