@@ -9,12 +9,15 @@
 // bf16 and written with TMA tensor stores from a 128-byte-swizzled staging
 // tile (so that every HBM write is a full, coalesced line).
 //
-// CTA = (128 query rows = one or two block-rows, one sender head); it walks the
-// ascending union of the kept block columns of its block-rows.  Warp roles as
-// in the statistics kernel: warp 0 TMA loads, warp 1 tcgen05 issue, warps 2-9
-// normalise and store (two per TMEM lane quadrant, one per half of the
-// block's columns).  The CTA also writes col_idx and the per-(block,
-// head) tile index used by the retrieval.
+// Persistent: two CTAs per SM at B = 64 (one at B = 128) walk the heavy-first
+// (128-row tile, sender head) item list.  Warp roles: warp 0 TMA loads (Q of
+// each item, K blocks through a ring that runs on across items), warp 1
+// tcgen05 issue, warps 2-9 normalise and store (two per TMEM lane quadrant,
+// one per half of the block's columns), warp 10 plans the next item while the
+// current one runs: the ascending union of its block-rows' kept columns, the
+// rows' statistics, and the col_idx / per-(block, head) tile index entries
+// used by the retrieval.  Plans are double-buffered, so item setup is off
+// the critical path.
 #include <cmath>
 
 #include "mf_internal.cuh"
@@ -32,17 +35,27 @@ struct PackLayout {
   static constexpr int kQBytes = kRows * D * 2;
   static constexpr int kKChunk = BLK * 128;            // BLK key rows x 64 bf16
   static constexpr int kKBytes = BLK * D * 2;
-  static constexpr int kStages = 3;  // with one staging buffer: still two CTAs per SM at B = 64
+  static constexpr int kStages = 3;
   static constexpr int kStageBytes = (BLK == 64) ? 2 * 64 * 128 : 2 * 128 * 128;  // one staging buffer
+  // plan of one item: union columns, their positions in the two kept lists,
+  // the rows' exponent offsets and inverse sums, and the item's scalars
+  static constexpr int kPlanInts = 3 * kMaxU + 2 * kRows + 8;
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + kQBytes;
   static constexpr int kStg = kK + kStages * kKBytes;
-  static constexpr int kU = kStg + kStageBytes;        // int [5][kMaxU]: union + two flag arrays
-  static constexpr int kBar = kU + 5 * kMaxU * 4;
-  static constexpr int kSlot = kBar + 16 * 8;
+  static constexpr int kPlan = kStg + kStageBytes;     // two plans
+  static constexpr int kFl = kPlan + 2 * kPlanInts * 4; // planner's two flag arrays
+  static constexpr int kBar = kFl + 2 * kMaxU * 4;
+  static constexpr int kSlot = kBar + 32 * 8;
   static constexpr int kMisc = kSlot + 8;
   static constexpr int kBytes = kMisc + 16 + 1024;
 };
+
+// Fields of a plan (int offsets).
+constexpr int kPlBj = 0, kPlPos0 = kMaxU, kPlPos1 = 2 * kMaxU, kPlM2 = 3 * kMaxU,
+              kPlInvl = 3 * kMaxU + kRows, kPlMeta = 3 * kMaxU + 2 * kRows;
+// meta: [0] n_u, [1] head, [2] seq_start, [3] L, [4] tile index in the
+// sequence, [5] row_ptr of block-row 0, [6] row_ptr of block-row 1
 
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int* err) {
   int ok = 1;
@@ -53,9 +66,19 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int* er
   return ok != 0;
 }
 
+// Item r of this CTA in a snake order over the heavy-first (tile, head) list:
+// round r takes items [r*G, r*G+G), forwards on even rounds and backwards on
+// odd ones.  -1 once the list is exhausted.
+__device__ __forceinline__ int pack_item(int r, int n_items) {
+  const int G = gridDim.x;
+  const int idx = r * G + ((r & 1) ? (G - 1 - static_cast<int>(blockIdx.x))
+                                    : static_cast<int>(blockIdx.x));
+  return idx < n_items ? idx : -1;
+}
+
 // Writer warps: two per TMEM lane quadrant, each normalising half of the
-// block's columns.
-constexpr int kPackThreads = 64 + 256;
+// block's columns; one planner warp.
+constexpr int kPackThreads = 64 + 256 + 32;
 
 template <int D, int BLK>
 __global__ void __launch_bounds__(kPackThreads, (BLK == 64) ? 2 : 1)
@@ -69,45 +92,23 @@ __global__ void __launch_bounds__(kPackThreads, (BLK == 64) ? 2 : 1)
                                              ~uintptr_t(1023));
   const uint32_t sb = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const RowTile tile = p.tiles[blockIdx.x];
-  const int h = blockIdx.y;
-  const int hk = h / (p.H_s / p.H_ks);
-  int* u_bj = reinterpret_cast<int*>(smem + Lay::kU);
-  int* u_pos0 = u_bj + kMaxU;
-  int* u_pos1 = u_pos0 + kMaxU;
-  int* fl0 = u_pos1 + kMaxU;  // position of column bj in kept list 0 (or -1)
-  int* fl1 = fl0 + kMaxU;
-  volatile int* misc = reinterpret_cast<volatile int*>(smem + Lay::kMisc);  // [0]=n_u [1]=abort
+  const int n_items = p.n_tiles * p.H_s;
+  auto plan = [&](int k) { return reinterpret_cast<int*>(smem + Lay::kPlan) + (k & 1) * Lay::kPlanInts; };
+  volatile int* misc = reinterpret_cast<volatile int*>(smem + Lay::kMisc);  // [1] = abort
 
   const uint32_t barQ = sb + Lay::kBar;
-  auto barFull = [&](int s) { return sb + Lay::kBar + 8u * (1 + s); };
-  auto barEmpty = [&](int s) { return sb + Lay::kBar + 8u * (1 + NS + s); };
-  auto barSFull = [&](int b) { return sb + Lay::kBar + 8u * (1 + 2 * NS + b); };
-  auto barSEmpty = [&](int b) { return sb + Lay::kBar + 8u * (3 + 2 * NS + b); };
-  const uint32_t barDone = sb + Lay::kBar + 8u * (5 + 2 * NS);
-
-  // block-rows covered by this tile
-  const int nsub = kRows / BLK;  // 2 for B=64, 1 for B=128
-  int rbv[2], kc[2], base[2];
-  const int* kl[2];
-  for (int t = 0; t < 2; ++t) {
-    const bool exists = t < nsub && (tile.tl * kRows + t * BLK) < tile.L;
-    rbv[t] = exists ? tile.rb0 + t : -1;
-    if (exists) {
-      const RowBlock rbk = p.rbs[rbv[t]];
-      const int row = h * p.R + rbv[t];
-      kc[t] = p.kcount[row];
-      base[t] = p.row_ptr[row];
-      kl[t] = p.keptcols + static_cast<size_t>(h) * p.C + rbk.cand_off;
-    } else {
-      kc[t] = 0;
-      base[t] = 0;
-      kl[t] = nullptr;
-    }
-  }
+  const uint32_t barQEmpty = sb + Lay::kBar + 8u;
+  auto barFull = [&](int s) { return sb + Lay::kBar + 8u * (2 + s); };
+  auto barEmpty = [&](int s) { return sb + Lay::kBar + 8u * (2 + NS + s); };
+  auto barSFull = [&](int b) { return sb + Lay::kBar + 8u * (2 + 2 * NS + b); };
+  auto barSEmpty = [&](int b) { return sb + Lay::kBar + 8u * (4 + 2 * NS + b); };
+  auto barReady = [&](int k) { return sb + Lay::kBar + 8u * (6 + 2 * NS + (k & 1)); };
+  auto barFree = [&](int k) { return sb + Lay::kBar + 8u * (8 + 2 * NS + (k & 1)); };
+  const uint32_t barDone = sb + Lay::kBar + 8u * (10 + 2 * NS);
 
   if (threadIdx.x == 0) {
     mbar_init(barQ, 1);
+    mbar_init(barQEmpty, 1);
     for (int s = 0; s < NS; ++s) {
       mbar_init(barFull(s), 1);
       mbar_init(barEmpty(s), 1);
@@ -115,108 +116,204 @@ __global__ void __launch_bounds__(kPackThreads, (BLK == 64) ? 2 : 1)
     for (int b = 0; b < 2; ++b) {
       mbar_init(barSFull(b), 1);
       mbar_init(barSEmpty(b), 8);
+      mbar_init(barReady(b), 1);
+      mbar_init(barFree(b), 10);  // loader, MMA issuer, eight writer warps
     }
     mbar_init(barDone, 1);
     fence_mbar_init();
     misc[1] = 0;
-  }
-  // ascending union of the two kept lists, in parallel: mark each list's
-  // columns, then compact with warp ballots
-  const int nbj = p.causal ? (tile.tl + 1) * (kRows / BLK) : (tile.L + BLK - 1) / BLK;
-  for (int i = threadIdx.x; i < kMaxU; i += blockDim.x) {
-    fl0[i] = -1;
-    fl1[i] = -1;
-  }
-  __syncthreads();
-  for (int t = 0; t < 2; ++t) {
-    if (rbv[t] < 0) continue;
-    const RowBlock rbk = p.rbs[rbv[t]];
-    int* fl = t ? fl1 : fl0;
-    for (int i = threadIdx.x; i < kc[t]; i += blockDim.x) {
-      const int bj = kl[t][i];
-      fl[bj] = i;
-      // col_idx and the retrieval's tile index of every kept (block, head)
-      p.col_idx[base[t] + i] = bj;
-      p.tile_of[static_cast<size_t>(rbk.cand_off + bj) * p.H_s + h] = base[t] + i;
-    }
-  }
-  __syncthreads();
-  if (warp == 0) {
-    int n = 0;
-    for (int c0 = 0; c0 < nbj; c0 += 32) {
-      const int bj = c0 + lane;
-      const int a = (bj < nbj) ? fl0[bj] : -1, b = (bj < nbj) ? fl1[bj] : -1;
-      const bool f = (a >= 0) || (b >= 0);
-      const uint32_t m = __ballot_sync(0xffffffffu, f);
-      if (f) {
-        const int pos = n + __popc(m & ((1u << lane) - 1u));
-        u_bj[pos] = bj;
-        u_pos0[pos] = a;
-        u_pos1[pos] = b;
-      }
-      n += __popc(m);
-    }
-    if (lane == 0) misc[0] = n;
   }
   if (warp == 1) tmem_alloc(sb + Lay::kSlot, 2 * kN < 32 ? 32 : 2 * kN);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + Lay::kSlot);
-  const int n_u = misc[0];
 
-  if (warp == 0) {
+  if (warp == 10) {
+    // ------------------------------------------------------------ planner
+    int* fl0 = reinterpret_cast<int*>(smem + Lay::kFl);  // position of column bj in kept list 0 (or -1)
+    int* fl1 = fl0 + kMaxU;
+    for (int k = 0;; ++k) {
+      const int idx = pack_item(k, n_items);
+      if (idx < 0 || misc[1]) break;
+      if (!warp_wait(barFree(k), ((k >> 1) & 1) ^ 1, p.err)) {
+        misc[1] = 1;
+        break;
+      }
+      const int ti = idx / p.H_s, h = idx - ti * p.H_s;
+      const RowTile tile = p.tiles[ti];
+      int* pl = plan(k);
+      const int nsub = kRows / BLK;  // 2 for B=64, 1 for B=128
+      int rbv[2], kc[2], base[2];
+      const int* kl[2];
+      for (int t = 0; t < 2; ++t) {
+        const bool exists = t < nsub && (tile.tl * kRows + t * BLK) < tile.L;
+        rbv[t] = exists ? tile.rb0 + t : -1;
+        kc[t] = 0;
+        base[t] = 0;
+        kl[t] = nullptr;
+        if (exists) {
+          const int row = h * p.R + rbv[t];
+          kc[t] = p.kcount[row];
+          base[t] = p.row_ptr[row];
+          kl[t] = p.keptcols + static_cast<size_t>(h) * p.C + p.rbs[rbv[t]].cand_off;
+        }
+      }
+      const int nbj = p.causal ? (tile.tl + 1) * (kRows / BLK) : (tile.L + BLK - 1) / BLK;
+      for (int i = lane; i < nbj; i += 32) {
+        fl0[i] = -1;
+        fl1[i] = -1;
+      }
+      __syncwarp();
+      for (int t = 0; t < 2; ++t) {
+        if (rbv[t] < 0) continue;
+        const int cand_off = p.rbs[rbv[t]].cand_off;
+        int* fl = t ? fl1 : fl0;
+        for (int i = lane; i < kc[t]; i += 32) {
+          const int bj = kl[t][i];
+          fl[bj] = i;
+          // col_idx and the retrieval's tile index of every kept (block, head)
+          p.col_idx[base[t] + i] = bj;
+          p.tile_of[static_cast<size_t>(cand_off + bj) * p.H_s + h] = base[t] + i;
+        }
+      }
+      __syncwarp();
+      int n = 0;
+      for (int c0 = 0; c0 < nbj; c0 += 32) {
+        const int bj = c0 + lane;
+        const int a = (bj < nbj) ? fl0[bj] : -1, b = (bj < nbj) ? fl1[bj] : -1;
+        const bool f = (a >= 0) || (b >= 0);
+        const uint32_t m = __ballot_sync(0xffffffffu, f);
+        if (f) {
+          const int pos = n + __popc(m & ((1u << lane) - 1u));
+          pl[kPlBj + pos] = bj;
+          pl[kPlPos0 + pos] = a;
+          pl[kPlPos1 + pos] = b;
+        }
+        n += __popc(m);
+      }
+      float* m2 = reinterpret_cast<float*>(pl + kPlM2);
+      float* invl = reinterpret_cast<float*>(pl + kPlInvl);
+      for (int r = lane; r < kRows; r += 32) {
+        const int row_local = tile.tl * kRows + r;
+        float mm = 0.f, il = 0.f;
+        if (n > 0 && row_local < tile.L) {
+          const size_t o = static_cast<size_t>(h) * p.T + tile.seq_start + row_local;
+          mm = p.row_max[o] * 1.4426950408889634f;
+          il = 1.f / p.row_sum[o];
+        }
+        m2[r] = mm;
+        invl[r] = il;
+      }
+      if (lane == 0) {
+        pl[kPlMeta + 0] = n;
+        pl[kPlMeta + 1] = h;
+        pl[kPlMeta + 2] = tile.seq_start;
+        pl[kPlMeta + 3] = tile.L;
+        pl[kPlMeta + 4] = tile.tl;
+        pl[kPlMeta + 5] = base[0];
+        pl[kPlMeta + 6] = base[1];
+      }
+      // the flags are rewritten for the next item only after every lane has
+      // read them; the plan is published by the arrive's release
+      __syncwarp();
+      if (lane == 0) mbar_arrive(barReady(k));
+    }
+  } else if (warp == 0) {
+    // ------------------------------------------------------------- loader
     if (lane == 0) {
       prefetch_tmap(&tq);
       prefetch_tmap(&tk);
       prefetch_tmap(&tvals);
-      if (n_u > 0) {
-        mbar_arrive_tx(barQ, Lay::kQBytes);
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_2d(sb + Lay::kQ + c * Lay::kQChunk, &tq, h * D + c * 64,
-                      tile.seq_start + tile.tl * kRows, barQ);
-      }
-      int issued = 0;
-      for (int u = 0; u < n_u; ++u) {
-        const int s = u % NS;
-        if (!mbar_wait(barEmpty(s), ((u / NS) & 1) ^ 1, p.err)) {
+      int g = 0, nq = 0;
+      for (int k = 0;; ++k) {
+        const int idx = pack_item(k, n_items);
+        if (idx < 0 || misc[1]) break;
+        if (!mbar_wait(barReady(k), (k >> 1) & 1, p.err)) {
           misc[1] = 1;
           break;
         }
-        mbar_arrive_tx(barFull(s), Lay::kKBytes);
-        const uint32_t dst = sb + Lay::kK + s * Lay::kKBytes;
+        const int* pl = plan(k);
+        const int n_u = pl[kPlMeta + 0], h = pl[kPlMeta + 1];
+        const int y0 = pl[kPlMeta + 2] + pl[kPlMeta + 4] * kRows;
+        const int hk = h / (p.H_s / p.H_ks);
+        bool ok = true;
+        if (n_u > 0) {
+          // Q of this item replaces the previous item's once its MMAs are done
+          if (!mbar_wait(barQEmpty, (nq & 1) ^ 1, p.err)) {
+            ok = false;
+          } else {
+            mbar_arrive_tx(barQ, Lay::kQBytes);
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_2d(dst + c * Lay::kKChunk, &tk, hk * D + c * 64,
-                      tile.seq_start + u_bj[u] * BLK, barFull(s));
-        issued = u + 1;
+            for (int c = 0; c < D / 64; ++c)
+              tma_load_2d(sb + Lay::kQ + c * Lay::kQChunk, &tq, h * D + c * 64, y0, barQ);
+            ++nq;
+          }
+        }
+        for (int u = 0; ok && u < n_u; ++u, ++g) {
+          const int s = g % NS;
+          if (!mbar_wait(barEmpty(s), ((g / NS) & 1) ^ 1, p.err)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_tx(barFull(s), Lay::kKBytes);
+          const uint32_t dst = sb + Lay::kK + s * Lay::kKBytes;
+          const int ky = pl[kPlMeta + 2] + pl[kPlBj + u] * BLK;
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c) tma_load_2d(dst + c * Lay::kKChunk, &tk, hk * D + c * 64, ky, barFull(s));
+        }
+        mbar_arrive(barFree(k));
+        if (!ok) {
+          misc[1] = 1;
+          break;
+        }
       }
-      for (int u = (issued > NS ? issued - NS : 0); u < issued; ++u)
-        mbar_wait(barFull(u % NS), (u / NS) & 1, nullptr);
-      if (n_u > 0) mbar_wait(barQ, 0, nullptr);
+      // drain: the last loads of every stage and the last Q
+      for (int u = (g > NS ? g - NS : 0); u < g; ++u) mbar_wait(barFull(u % NS), (u / NS) & 1, nullptr);
+      if (nq > 0) mbar_wait(barQ, (nq - 1) & 1, nullptr);
     }
   } else if (warp == 1) {
+    // --------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(kRows, kN, false, false);
-      bool ok = (n_u == 0) || mbar_wait(barQ, 0, p.err);
-      for (int u = 0; ok && u < n_u; ++u) {
-        const int s = u % NS, b = u & 1;
-        if (!mbar_wait(barFull(s), (u / NS) & 1, p.err) ||
-            !mbar_wait(barSEmpty(b), ((u >> 1) & 1) ^ 1, p.err)) {
+      int g = 0, nq = 0;
+      for (int k = 0;; ++k) {
+        const int idx = pack_item(k, n_items);
+        if (idx < 0 || misc[1]) break;
+        if (!mbar_wait(barReady(k), (k >> 1) & 1, p.err)) {
           misc[1] = 1;
           break;
         }
-        tc_fence_after();
-        const uint32_t qa = sb + Lay::kQ, ka = sb + Lay::kK + s * Lay::kKBytes;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          tc_mma(tmem + b * kN, sdesc_sw128(qa + (kk >> 2) * Lay::kQChunk + (kk & 3) * 32, 16, 1024),
-                 sdesc_sw128(ka + (kk >> 2) * Lay::kKChunk + (kk & 3) * 32, 16, 1024), idesc,
-                 kk > 0 ? 1u : 0u);
+        const int n_u = plan(k)[kPlMeta + 0];
+        mbar_arrive(barFree(k));
+        bool ok = true;
+        if (n_u > 0) {
+          ok = mbar_wait(barQ, nq & 1, p.err);
+          ++nq;
         }
-        tc_commit(barEmpty(s));
-        tc_commit(barSFull(b));
+        for (int u = 0; ok && u < n_u; ++u, ++g) {
+          const int s = g % NS, b = g & 1;
+          if (!mbar_wait(barFull(s), (g / NS) & 1, p.err) ||
+              !mbar_wait(barSEmpty(b), ((g >> 1) & 1) ^ 1, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t qa = sb + Lay::kQ, ka = sb + Lay::kK + s * Lay::kKBytes;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            tc_mma(tmem + b * kN, sdesc_sw128(qa + (kk >> 2) * Lay::kQChunk + (kk & 3) * 32, 16, 1024),
+                   sdesc_sw128(ka + (kk >> 2) * Lay::kKChunk + (kk & 3) * 32, 16, 1024), idesc,
+                   kk > 0 ? 1u : 0u);
+          }
+          tc_commit(barEmpty(s));
+          tc_commit(barSFull(b));
+        }
+        if (!ok) {
+          misc[1] = 1;
+          break;
+        }
+        if (n_u > 0) tc_commit(barQEmpty);  // Q may be replaced once these MMAs finish
       }
       tc_commit(barDone);
       mbar_wait(barDone, 0, nullptr);
@@ -227,99 +324,110 @@ __global__ void __launch_bounds__(kPackThreads, (BLK == 64) ? 2 : 1)
     const int wq = warp & 3;
     const int ch = (warp - 2) >> 2;     // column half of this warp
     const int row = wq * 32 + lane;
-    const int row_local = tile.tl * kRows + row;
-    const bool row_ok = row_local < tile.L;
     const int sub = row / BLK;  // which block-row of the tile
     const int rloc = row - sub * BLK;
     const uint32_t trow = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     const float sc = p.scale_log2;
-    float m2 = 0.f, invl = 0.f;
-    if (row_ok) {
-      const size_t o = static_cast<size_t>(h) * p.T + tile.seq_start + row_local;
-      m2 = p.row_max[o] * 1.4426950408889634f;
-      invl = 1.f / p.row_sum[o];
-    }
-    // staging: BLK=64 -> per buffer two 8 KB tiles (one per block-row);
-    //          BLK=128 -> per buffer one 32 KB tile as two 64-column boxes
+    // staging: BLK=64 -> two 8 KB tiles (one per block-row);
+    //          BLK=128 -> one 32 KB tile as two 64-column boxes
     const uint32_t stg = sb + Lay::kStg;
     uint8_t* stg_g = smem + Lay::kStg;
-    constexpr int kBuf = Lay::kStageBytes;
     const int grp_threads = (BLK == 64) ? 128 : 256;
     const int bar_id = (BLK == 64) ? 2 + sub : 2;
     const bool leader = ((BLK == 64) ? (rloc == 0) : (row == 0)) && ch == 0;
-    const float2 sc2 = make_float2(sc, sc), nm2 = make_float2(-m2, -m2), il2 = make_float2(invl, invl);
-    int nstore = 0;
-    for (int u = 0; u < n_u; ++u) {
-      const int b = u & 1;
-      if (!warp_wait(barSFull(b), (u >> 1) & 1, p.err)) break;
-      tc_fence_after();
-      float s[kHalfCols];
-      {
-        uint32_t* r = reinterpret_cast<uint32_t*>(s);
-#pragma unroll
-        for (int c = 0; c < kHalfCols; c += 32) tmem_ld32(trow + b * kN + ch * kHalfCols + c, r + c);
-      }
-      tc_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(barSEmpty(b));
-      const int pos = (sub == 0) ? u_pos0[u] : u_pos1[u];
-      if (pos < 0) continue;  // this block-row does not keep the block (group-uniform)
-      const int bj = u_bj[u];
-      const int sbuf = 0;
-      ++nstore;
-      // the store issued from the staging buffer one tile ago must have
-      // finished reading it (one buffer leaves room for a third K stage)
-      if (leader) bulk_wait_read_0();
-      named_bar(bar_id, grp_threads);
-      // only the diagonal block and the sequence's last block need masking
-      const bool edge = !row_ok || (bj * BLK + BLK > tile.L) ||
-                        (p.causal && bj * BLK + BLK - 1 > tile.tl * kRows + (row - rloc));
-      const int c_base = ch * kHalfCols;
-#pragma unroll
-      for (int c8 = 0; c8 < kHalfCols / 8; ++c8) {
-        float v[8];
-#pragma unroll
-        for (int e = 0; e < 8; e += 2) {
-          float2 t = ffma2(make_float2(s[c8 * 8 + e], s[c8 * 8 + e + 1]), sc2, nm2);
-          t.x = ex2(t.x);
-          t.y = ex2(t.y);
-          t = fmul2(t, il2);
-          v[e] = t.x;
-          v[e + 1] = t.y;
+    const float2 sc2 = make_float2(sc, sc);
+    int g = 0;
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      const int idx = pack_item(k, n_items);
+      if (idx < 0 || misc[1]) break;
+      if (!warp_wait(barReady(k), (k >> 1) & 1, p.err)) break;
+      const int* pl = plan(k);
+      const int n_u = pl[kPlMeta + 0];
+      const int L = pl[kPlMeta + 3], tl = pl[kPlMeta + 4];
+      const int base_sub = pl[kPlMeta + 5 + sub];
+      const int* u_pos = pl + (sub == 0 ? kPlPos0 : kPlPos1);
+      const int row_local = tl * kRows + row;
+      const bool row_ok = row_local < L;
+      const float m2 = reinterpret_cast<const float*>(pl + kPlM2)[row];
+      const float invl = reinterpret_cast<const float*>(pl + kPlInvl)[row];
+      const float2 nm2 = make_float2(-m2, -m2), il2 = make_float2(invl, invl);
+      for (int u = 0; u < n_u; ++u, ++g) {
+        const int b = g & 1;
+        if (!warp_wait(barSFull(b), (g >> 1) & 1, p.err)) {
+          ok = false;
+          break;
         }
-        if (edge) {
+        tc_fence_after();
+        float s[kHalfCols];
+        {
+          uint32_t* r = reinterpret_cast<uint32_t*>(s);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int j = bj * BLK + c_base + c8 * 8 + e;
-            const bool vis = row_ok && (j < tile.L) && (!p.causal || j <= row_local);
-            if (!vis) v[e] = 0.f;
+          for (int c = 0; c < kHalfCols; c += 32) tmem_ld32(trow + b * kN + ch * kHalfCols + c, r + c);
+        }
+        tc_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(barSEmpty(b));
+        const int pos = u_pos[u];
+        if (pos < 0) continue;  // this block-row does not keep the block (group-uniform)
+        const int bj = pl[kPlBj + u];
+        // the store issued from the staging buffer one tile ago must have
+        // finished reading it
+        if (leader) bulk_wait_read_0();
+        named_bar(bar_id, grp_threads);
+        // only the diagonal block and the sequence's last block need masking
+        const bool edge = !row_ok || (bj * BLK + BLK > L) ||
+                          (p.causal && bj * BLK + BLK - 1 > tl * kRows + (row - rloc));
+        const int c_base = ch * kHalfCols;
+#pragma unroll
+        for (int c8 = 0; c8 < kHalfCols / 8; ++c8) {
+          float v[8];
+#pragma unroll
+          for (int e = 0; e < 8; e += 2) {
+            float2 t = ffma2(make_float2(s[c8 * 8 + e], s[c8 * 8 + e + 1]), sc2, nm2);
+            t.x = ex2(t.x);
+            t.y = ex2(t.y);
+            t = fmul2(t, il2);
+            v[e] = t.x;
+            v[e + 1] = t.y;
           }
+          if (edge) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int j = bj * BLK + c_base + c8 * 8 + e;
+              const bool vis = row_ok && (j < L) && (!p.causal || j <= row_local);
+              if (!vis) v[e] = 0.f;
+            }
+          }
+          uint4 w;
+          w.x = pack_bf16x2(v[0], v[1]);
+          w.y = pack_bf16x2(v[2], v[3]);
+          w.z = pack_bf16x2(v[4], v[5]);
+          w.w = pack_bf16x2(v[6], v[7]);
+          const int cc = (c_base >> 3) + c8;  // 16-byte chunk in the B-column row
+          uint32_t off;
+          if (BLK == 64) off = sub * 8192 + sw128_off(rloc, cc);
+          else off = (cc >> 3) * 16384 + sw128_off(row, cc & 7);
+          *reinterpret_cast<uint4*>(stg_g + off) = w;
         }
-        uint4 w;
-        w.x = pack_bf16x2(v[0], v[1]);
-        w.y = pack_bf16x2(v[2], v[3]);
-        w.z = pack_bf16x2(v[4], v[5]);
-        w.w = pack_bf16x2(v[6], v[7]);
-        const int cc = (c_base >> 3) + c8;  // 16-byte chunk in the B-column row
-        uint32_t off;
-        if (BLK == 64) off = sbuf * kBuf + sub * 8192 + sw128_off(rloc, cc);
-        else off = sbuf * kBuf + (cc >> 3) * 16384 + sw128_off(row, cc & 7);
-        *reinterpret_cast<uint4*>(stg_g + off) = w;
-      }
-      fence_async_smem();
-      named_bar(bar_id, grp_threads);
-      if (leader) {
-        const int tidx = ((sub == 0) ? base[0] : base[1]) + pos;
-        if (BLK == 64) {
-          tma_store_2d(&tvals, stg + sbuf * kBuf + sub * 8192, 0, tidx * 64);
-        } else {
-          tma_store_2d(&tvals, stg + sbuf * kBuf, 0, tidx * 128);
-          tma_store_2d(&tvals, stg + sbuf * kBuf + 16384, 64, tidx * 128);
+        fence_async_smem();
+        named_bar(bar_id, grp_threads);
+        if (leader) {
+          const int tidx = base_sub + pos;
+          if (BLK == 64) {
+            tma_store_2d(&tvals, stg + sub * 8192, 0, tidx * 64);
+          } else {
+            tma_store_2d(&tvals, stg, 0, tidx * 128);
+            tma_store_2d(&tvals, stg + 16384, 64, tidx * 128);
+          }
+          bulk_commit();
         }
-        bulk_commit();
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(barFree(k));
     }
+    if (!ok) misc[1] = 1;
     if (leader) bulk_wait_all();
   }
   tc_fence_before();
@@ -338,7 +446,14 @@ cudaError_t launch_pack_t(const CompressParams& p, const CUtensorMap& tq, const 
   const int smem = PackLayout<D, BLK>::kBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(p.n_tiles, p.H_s);
+  int sms = 0;
+  e = sm_count(&sms);
+  if (e != cudaSuccess) return e;
+  const long long items = static_cast<long long>(p.n_tiles) * p.H_s;
+  if (items <= 0) return cudaSuccess;
+  // persistent: two CTAs per SM at B = 64 (one at B = 128)
+  const long long slots = static_cast<long long>(sms) * ((BLK == 64) ? 2 : 1);
+  const int grid = static_cast<int>(items < slots ? items : slots);
   kern<<<grid, kPackThreads, smem, s>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
