@@ -61,7 +61,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // 2-D bf16 map: `inner` elements per row, `rows` rows, `stride` bytes between
 // rows; box = box_inner x box_rows; 128-byte swizzle; out-of-range reads give 0.
 int make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t stride,
-             uint32_t box_inner, uint32_t box_rows) {
+             uint32_t box_inner, uint32_t box_rows,
+             CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   auto fn = encode_fn();
   if (!fn) return fail(MF_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable (driver too old?)");
   cuuint64_t dims[2] = {inner, rows};
@@ -69,7 +70,7 @@ int make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, ui
   cuuint32_t box[2] = {box_inner, box_rows};
   cuuint32_t es[2] = {1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
-                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(MF_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
   return MF_OK;
@@ -473,8 +474,9 @@ int mf_compress(mf_bsr_t h, int layer, const void* q, const void* k, int dtype, 
   if (cap > 0) {
     if (dtype == MF_DTYPE_BF16) {
       CUtensorMap tvals{};
-      if ((rc = make_map(&tvals, L.values, B, (uint64_t)cap * B, (uint64_t)B * 2, 64,
-                         B == 64 ? 64 : 128)) != MF_OK)
+      // the pack kernel's writer warps each store 32 rows x B/2 columns
+      if ((rc = make_map(&tvals, L.values, B, (uint64_t)cap * B, (uint64_t)B * 2, B / 2, 32,
+                         B == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B)) != MF_OK)
         return rc;
       MF_CUDA(timed(h, MF_K_PACK, s, [&] { return launch_pack_bf16(cp, tq, tk_pack, tvals, s); }),
               "pack kernel");

@@ -5,15 +5,17 @@
 // "Practical Implementation Details": the filtered map is stored in a compact
 // Block Sparse Row layout.  Row statistics m_i, l_i come from the statistics
 // pass; here only the kept tiles are recomputed (Q.K^T on tcgen05 into TMEM),
-// normalised, P_ij = 2^(s_ij*log2(e)/sqrt(d) - m_i*log2(e)) / l_i, rounded to
-// bf16 and written with TMA tensor stores from a 128-byte-swizzled staging
-// tile (so that every HBM write is a full, coalesced line).
+// normalised, P_ij = 2^(s_ij*log2(e)/sqrt(d) - m_i*log2(e) - log2(l_i)),
+// rounded to bf16 and written with TMA tensor stores from swizzled staging
+// buffers (so that every HBM write is a full, coalesced line).
 //
 // Persistent: two CTAs per SM at B = 64 (one at B = 128) walk the heavy-first
 // (128-row tile, sender head) item list.  Warp roles: warp 0 TMA loads (Q of
 // each item, K blocks through a ring that runs on across items), warp 1
 // tcgen05 issue, warps 2-9 normalise and store (two per TMEM lane quadrant,
-// one per half of the block's columns), warp 10 plans the next item while the
+// one per half of the block's columns; each warp stages its 32 x B/2 slice in
+// its own swizzled buffer and issues its own TMA store, so the writer warps
+// never wait on one another), warp 10 plans the next item while the
 // current one runs: the ascending union of its block-rows' kept columns, the
 // rows' statistics, and the col_idx / per-(block, head) tile index entries
 // used by the retrieval.  Plans are double-buffered, so item setup is off
@@ -36,10 +38,11 @@ struct PackLayout {
   static constexpr int kKChunk = BLK * 128;            // BLK key rows x 64 bf16
   static constexpr int kKBytes = BLK * D * 2;
   static constexpr int kStages = 3;
-  static constexpr int kStageBytes = (BLK == 64) ? 2 * 64 * 128 : 2 * 128 * 128;  // one staging buffer
+  static constexpr int kWarpStage = 32 * BLK;           // one writer warp's 32 rows x BLK/2 bf16
+  static constexpr int kStageBytes = 8 * kWarpStage;
   // plan of one item: union columns, their positions in the two kept lists,
-  // the rows' exponent offsets and inverse sums, and the item's scalars
-  static constexpr int kPlanInts = 3 * kMaxU + 2 * kRows + 8;
+  // the rows' exponent offsets, and the item's scalars
+  static constexpr int kPlanInts = 3 * kMaxU + kRows + 8;
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + kQBytes;
   static constexpr int kStg = kK + kStages * kKBytes;
@@ -53,7 +56,7 @@ struct PackLayout {
 
 // Fields of a plan (int offsets).
 constexpr int kPlBj = 0, kPlPos0 = kMaxU, kPlPos1 = 2 * kMaxU, kPlM2 = 3 * kMaxU,
-              kPlInvl = 3 * kMaxU + kRows, kPlMeta = 3 * kMaxU + 2 * kRows;
+              kPlMeta = 3 * kMaxU + kRows;
 // meta: [0] n_u, [1] head, [2] seq_start, [3] L, [4] tile index in the
 // sequence, [5] row_ptr of block-row 0, [6] row_ptr of block-row 1
 
@@ -192,18 +195,17 @@ __global__ void __launch_bounds__(kPackThreads, (BLK == 64) ? 2 : 1)
         }
         n += __popc(m);
       }
+      // exponent offset of each row: m_i log2(e) + log2(l_i), so that the
+      // division by the row sum folds into the exp2
       float* m2 = reinterpret_cast<float*>(pl + kPlM2);
-      float* invl = reinterpret_cast<float*>(pl + kPlInvl);
       for (int r = lane; r < kRows; r += 32) {
         const int row_local = tile.tl * kRows + r;
-        float mm = 0.f, il = 0.f;
+        float mm = 0.f;
         if (n > 0 && row_local < tile.L) {
           const size_t o = static_cast<size_t>(h) * p.T + tile.seq_start + row_local;
-          mm = p.row_max[o] * 1.4426950408889634f;
-          il = 1.f / p.row_sum[o];
+          mm = p.row_max[o] * 1.4426950408889634f + log2f(p.row_sum[o]);
         }
         m2[r] = mm;
-        invl[r] = il;
       }
       if (lane == 0) {
         pl[kPlMeta + 0] = n;
@@ -325,16 +327,13 @@ __global__ void __launch_bounds__(kPackThreads, (BLK == 64) ? 2 : 1)
     const int ch = (warp - 2) >> 2;     // column half of this warp
     const int row = wq * 32 + lane;
     const int sub = row / BLK;  // which block-row of the tile
-    const int rloc = row - sub * BLK;
+    const int rloc0 = wq * 32 - sub * BLK;  // the warp's first row in its block-row
     const uint32_t trow = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     const float sc = p.scale_log2;
-    // staging: BLK=64 -> two 8 KB tiles (one per block-row);
-    //          BLK=128 -> one 32 KB tile as two 64-column boxes
-    const uint32_t stg = sb + Lay::kStg;
-    uint8_t* stg_g = smem + Lay::kStg;
-    const int grp_threads = (BLK == 64) ? 128 : 256;
-    const int bar_id = (BLK == 64) ? 2 + sub : 2;
-    const bool leader = ((BLK == 64) ? (rloc == 0) : (row == 0)) && ch == 0;
+    // this warp's staging buffer: 32 rows of BLK/2 bf16 in the layout of the
+    // store map's swizzle (64-byte rows at B = 64, 128-byte rows at B = 128)
+    const uint32_t wstg = sb + Lay::kStg + (warp - 2) * Lay::kWarpStage;
+    uint8_t* wstg_g = smem + Lay::kStg + (warp - 2) * Lay::kWarpStage;
     const float2 sc2 = make_float2(sc, sc);
     int g = 0;
     bool ok = true;
@@ -350,8 +349,7 @@ __global__ void __launch_bounds__(kPackThreads, (BLK == 64) ? 2 : 1)
       const int row_local = tl * kRows + row;
       const bool row_ok = row_local < L;
       const float m2 = reinterpret_cast<const float*>(pl + kPlM2)[row];
-      const float invl = reinterpret_cast<const float*>(pl + kPlInvl)[row];
-      const float2 nm2 = make_float2(-m2, -m2), il2 = make_float2(invl, invl);
+      const float2 nm2 = make_float2(-m2, -m2);
       for (int u = 0; u < n_u; ++u, ++g) {
         const int b = g & 1;
         if (!warp_wait(barSFull(b), (g >> 1) & 1, p.err)) {
@@ -370,15 +368,15 @@ __global__ void __launch_bounds__(kPackThreads, (BLK == 64) ? 2 : 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(barSEmpty(b));
         const int pos = u_pos[u];
-        if (pos < 0) continue;  // this block-row does not keep the block (group-uniform)
+        if (pos < 0) continue;  // this block-row does not keep the block (warp-uniform)
         const int bj = pl[kPlBj + u];
-        // the store issued from the staging buffer one tile ago must have
+        // the store issued from this warp's buffer one tile ago must have
         // finished reading it
-        if (leader) bulk_wait_read_0();
-        named_bar(bar_id, grp_threads);
+        if (lane == 0) bulk_wait_read_0();
+        __syncwarp();
         // only the diagonal block and the sequence's last block need masking
         const bool edge = !row_ok || (bj * BLK + BLK > L) ||
-                          (p.causal && bj * BLK + BLK - 1 > tl * kRows + (row - rloc));
+                          (p.causal && bj * BLK + BLK - 1 > tl * kRows + sub * BLK);
         const int c_base = ch * kHalfCols;
 #pragma unroll
         for (int c8 = 0; c8 < kHalfCols / 8; ++c8) {
@@ -386,11 +384,8 @@ __global__ void __launch_bounds__(kPackThreads, (BLK == 64) ? 2 : 1)
 #pragma unroll
           for (int e = 0; e < 8; e += 2) {
             float2 t = ffma2(make_float2(s[c8 * 8 + e], s[c8 * 8 + e + 1]), sc2, nm2);
-            t.x = ex2(t.x);
-            t.y = ex2(t.y);
-            t = fmul2(t, il2);
-            v[e] = t.x;
-            v[e + 1] = t.y;
+            v[e] = ex2(t.x);
+            v[e + 1] = ex2(t.y);
           }
           if (edge) {
 #pragma unroll
@@ -405,22 +400,15 @@ __global__ void __launch_bounds__(kPackThreads, (BLK == 64) ? 2 : 1)
           w.y = pack_bf16x2(v[2], v[3]);
           w.z = pack_bf16x2(v[4], v[5]);
           w.w = pack_bf16x2(v[6], v[7]);
-          const int cc = (c_base >> 3) + c8;  // 16-byte chunk in the B-column row
           uint32_t off;
-          if (BLK == 64) off = sub * 8192 + sw128_off(rloc, cc);
-          else off = (cc >> 3) * 16384 + sw128_off(row, cc & 7);
-          *reinterpret_cast<uint4*>(stg_g + off) = w;
+          if (BLK == 64) off = lane * 64 + ((c8 ^ ((lane >> 1) & 3)) << 4);  // 64-byte swizzle
+          else off = sw128_off(lane, c8);                                     // 128-byte swizzle
+          *reinterpret_cast<uint4*>(wstg_g + off) = w;
         }
         fence_async_smem();
-        named_bar(bar_id, grp_threads);
-        if (leader) {
-          const int tidx = base_sub + pos;
-          if (BLK == 64) {
-            tma_store_2d(&tvals, stg + sub * 8192, 0, tidx * 64);
-          } else {
-            tma_store_2d(&tvals, stg, 0, tidx * 128);
-            tma_store_2d(&tvals, stg + 16384, 64, tidx * 128);
-          }
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&tvals, wstg, c_base, (base_sub + pos) * BLK + rloc0);
           bulk_commit();
         }
       }
@@ -428,7 +416,7 @@ __global__ void __launch_bounds__(kPackThreads, (BLK == 64) ? 2 : 1)
       if (lane == 0) mbar_arrive(barFree(k));
     }
     if (!ok) misc[1] = 1;
-    if (leader) bulk_wait_all();
+    if (lane == 0) bulk_wait_all();
   }
   tc_fence_before();
   __syncthreads();
