@@ -413,6 +413,7 @@ int mf_compress(mf_bsr_t h, int layer, const void* q, const void* k, int dtype, 
   cp.union_list = L.union_list;
   cp.utile = L.utile;
   cp.nnz_out = L.nnz_dev;
+  cp.pack_ctr = reinterpret_cast<int*>(L.nnz_dev + 1);  // in the 256-byte scalar slot
   cp.err = h->err_d;
 
   CUtensorMap tq{}, tk{}, tk_pack{};

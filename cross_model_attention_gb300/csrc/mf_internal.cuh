@@ -53,6 +53,7 @@ struct CompressParams {
   int* union_list;  // [C]
   int* utile;       // [C][H_s]  tile_of in union order: row cand_off + j is union column j
   long long* nnz_out;  // device scalar
+  int* pack_ctr;    // device scalar: the pack kernel's next item (reset by the scan kernel)
   int* err;
 };
 

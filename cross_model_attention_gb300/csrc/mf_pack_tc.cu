@@ -9,8 +9,10 @@
 // rounded to bf16 and written with TMA tensor stores from swizzled staging
 // buffers (so that every HBM write is a full, coalesced line).
 //
-// Persistent: two CTAs per SM at B = 64 (one at B = 128) walk the heavy-first
-// (128-row tile, sender head) item list.  Warp roles: warp 0 TMA loads (Q of
+// Persistent: two CTAs per SM at B = 64 (one at B = 128) take (128-row tile,
+// sender head) items from a global counter, heaviest tiles first, so the
+// last items taken are light ones whatever the kept blocks make each item
+// cost.  Warp roles: warp 0 TMA loads (Q of
 // each item, K blocks through a ring that runs on across items), warp 1
 // tcgen05 issue, warps 2-9 normalise and store (two per TMEM lane quadrant,
 // one per half of the block's columns; each warp stages its 32 x B/2 slice in
@@ -57,8 +59,8 @@ struct PackLayout {
 // Fields of a plan (int offsets).
 constexpr int kPlBj = 0, kPlPos0 = kMaxU, kPlPos1 = 2 * kMaxU, kPlM2 = 3 * kMaxU,
               kPlMeta = 3 * kMaxU + kRows;
-// meta: [0] n_u, [1] head, [2] seq_start, [3] L, [4] tile index in the
-// sequence, [5] row_ptr of block-row 0, [6] row_ptr of block-row 1
+// meta: [0] n_u (-1: no more items), [1] head, [2] seq_start, [3] L, [4] tile
+// index in the sequence, [5] row_ptr of block-row 0, [6] row_ptr of block-row 1
 
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int* err) {
   int ok = 1;
@@ -69,15 +71,6 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int* er
   return ok != 0;
 }
 
-// Item r of this CTA in a snake order over the heavy-first (tile, head) list:
-// round r takes items [r*G, r*G+G), forwards on even rounds and backwards on
-// odd ones.  -1 once the list is exhausted.
-__device__ __forceinline__ int pack_item(int r, int n_items) {
-  const int G = gridDim.x;
-  const int idx = r * G + ((r & 1) ? (G - 1 - static_cast<int>(blockIdx.x))
-                                    : static_cast<int>(blockIdx.x));
-  return idx < n_items ? idx : -1;
-}
 
 // Writer warps: two per TMEM lane quadrant, each normalising half of the
 // block's columns; one planner warp.
@@ -137,15 +130,26 @@ __global__ void __launch_bounds__(kPackThreads, (BLK == 64) ? 2 : 1)
     int* fl0 = reinterpret_cast<int*>(smem + Lay::kFl);  // position of column bj in kept list 0 (or -1)
     int* fl1 = fl0 + kMaxU;
     for (int k = 0;; ++k) {
-      const int idx = pack_item(k, n_items);
-      if (idx < 0 || misc[1]) break;
+      if (misc[1]) break;
       if (!warp_wait(barFree(k), ((k >> 1) & 1) ^ 1, p.err)) {
         misc[1] = 1;
         break;
       }
+      int* pl = plan(k);
+      int idx = 0;
+      if (lane == 0) idx = atomicAdd(p.pack_ctr, 1);
+      idx = __shfl_sync(0xffffffffu, idx, 0);
+      if (idx >= n_items) {
+        // no more items: an empty plan tells the other roles to stop
+        if (lane == 0) {
+          pl[kPlMeta + 0] = -1;
+          mbar_arrive(barReady(k));
+        }
+        break;
+      }
+      // item idx: tile idx / H_s of the heavy-first tile list, head idx % H_s
       const int ti = idx / p.H_s, h = idx - ti * p.H_s;
       const RowTile tile = p.tiles[ti];
-      int* pl = plan(k);
       const int nsub = kRows / BLK;  // 2 for B=64, 1 for B=128
       int rbv[2], kc[2], base[2];
       const int* kl[2];
@@ -229,14 +233,14 @@ __global__ void __launch_bounds__(kPackThreads, (BLK == 64) ? 2 : 1)
       prefetch_tmap(&tvals);
       int g = 0, nq = 0;
       for (int k = 0;; ++k) {
-        const int idx = pack_item(k, n_items);
-        if (idx < 0 || misc[1]) break;
+        if (misc[1]) break;
         if (!mbar_wait(barReady(k), (k >> 1) & 1, p.err)) {
           misc[1] = 1;
           break;
         }
         const int* pl = plan(k);
         const int n_u = pl[kPlMeta + 0], h = pl[kPlMeta + 1];
+        if (n_u < 0) break;
         const int y0 = pl[kPlMeta + 2] + pl[kPlMeta + 4] * kRows;
         const int hk = h / (p.H_s / p.H_ks);
         bool ok = true;
@@ -280,13 +284,13 @@ __global__ void __launch_bounds__(kPackThreads, (BLK == 64) ? 2 : 1)
       constexpr uint32_t idesc = idesc_bf16_f32(kRows, kN, false, false);
       int g = 0, nq = 0;
       for (int k = 0;; ++k) {
-        const int idx = pack_item(k, n_items);
-        if (idx < 0 || misc[1]) break;
+        if (misc[1]) break;
         if (!mbar_wait(barReady(k), (k >> 1) & 1, p.err)) {
           misc[1] = 1;
           break;
         }
         const int n_u = plan(k)[kPlMeta + 0];
+        if (n_u < 0) break;
         mbar_arrive(barFree(k));
         bool ok = true;
         if (n_u > 0) {
@@ -338,11 +342,11 @@ __global__ void __launch_bounds__(kPackThreads, (BLK == 64) ? 2 : 1)
     int g = 0;
     bool ok = true;
     for (int k = 0; ok; ++k) {
-      const int idx = pack_item(k, n_items);
-      if (idx < 0 || misc[1]) break;
+      if (misc[1]) break;
       if (!warp_wait(barReady(k), (k >> 1) & 1, p.err)) break;
       const int* pl = plan(k);
       const int n_u = pl[kPlMeta + 0];
+      if (n_u < 0) break;
       const int L = pl[kPlMeta + 3], tl = pl[kPlMeta + 4];
       const int base_sub = pl[kPlMeta + 5 + sub];
       const int* u_pos = pl + (sub == 0 ? kPlPos0 : kPlPos1);

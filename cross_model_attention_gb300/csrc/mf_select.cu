@@ -157,6 +157,7 @@ constexpr int kScanThreads = 1024;
 __global__ void __launch_bounds__(kScanThreads) scan_kernel(const CompressParams p) {
   __shared__ long long wsum[kScanThreads / 32];
   __shared__ long long carry_s;
+  if (threadIdx.x == 0 && p.pack_ctr) *p.pack_ctr = 0;  // the pack kernel's item counter
   const int n = p.H_s * p.R;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) carry_s = 0;
