@@ -414,6 +414,7 @@ int mf_compress(mf_bsr_t h, int layer, const void* q, const void* k, int dtype, 
   cp.utile = L.utile;
   cp.nnz_out = L.nnz_dev;
   cp.pack_ctr = reinterpret_cast<int*>(L.nnz_dev + 1);  // in the 256-byte scalar slot
+  cp.sel_done = reinterpret_cast<int*>(L.nnz_dev + 1) + 1;
   cp.err = h->err_d;
 
   CUtensorMap tq{}, tk{}, tk_pack{};
@@ -432,7 +433,6 @@ int mf_compress(mf_bsr_t h, int layer, const void* q, const void* k, int dtype, 
             "statistics kernel (fp32)");
   }
   MF_CUDA(timed(h, MF_K_SELECT, s, [&] { return launch_select(cp, s); }), "selection kernel");
-  MF_CUDA(timed(h, MF_K_SCAN, s, [&] { return launch_scan(cp, s); }), "row_ptr scan kernel");
   long long cap;
   if (h->exact_alloc) {
     // exact size: learn nnz first (the one host round trip of this mode)
@@ -469,9 +469,13 @@ int mf_compress(mf_bsr_t h, int layer, const void* q, const void* k, int dtype, 
     return fail(MF_ERR_OOM, "allocation of %zu bytes for the BSR values failed", L.values_bytes);
   }
   cp.col_idx = L.col_idx;
-  MF_CUDA(cudaMemsetAsync(L.tile_of, 0xFF, HC * 4, s), "tile index reset");
-  MF_CUDA(cudaMemsetAsync(reinterpret_cast<char*>(L.values) + L.values_bytes, 0, (size_t)B * B * 2, s),
-          "zero tile");
+  // the bf16 pack kernel writes the zero tile itself; the selection kernel
+  // has reset every candidate's tile index
+  if (dtype != MF_DTYPE_BF16 || cap == 0)
+    MF_CUDA(cudaMemsetAsync(reinterpret_cast<char*>(L.values) + L.values_bytes, 0, (size_t)B * B * 2, s),
+            "zero tile");
+  else
+    cp.zero_tile = reinterpret_cast<uint16_t*>(reinterpret_cast<char*>(L.values) + L.values_bytes);
   if (cap > 0) {
     if (dtype == MF_DTYPE_BF16) {
       CUtensorMap tvals{};

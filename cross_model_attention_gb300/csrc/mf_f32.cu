@@ -28,6 +28,7 @@ template <int D, int BLK>
 __global__ void __launch_bounds__(BLK) stats_f32_kernel(const CompressParams p,
                                                         const float* __restrict__ q,
                                                         const float* __restrict__ k) {
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0 && p.sel_done) *p.sel_done = 0;
   __shared__ float sk[BLK * D];
   __shared__ float red[BLK];
   const int rb = blockIdx.x, h = blockIdx.y;

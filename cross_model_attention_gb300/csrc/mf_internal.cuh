@@ -53,7 +53,9 @@ struct CompressParams {
   int* union_list;  // [C]
   int* utile;       // [C][H_s]  tile_of in union order: row cand_off + j is union column j
   long long* nnz_out;  // device scalar
-  int* pack_ctr;    // device scalar: the pack kernel's next item (reset by the scan kernel)
+  int* pack_ctr;    // device scalar: the pack kernel's next item (reset by the selection kernel)
+  int* sel_done;    // device scalar: selection CTAs finished (reset by the statistics kernel)
+  uint16_t* zero_tile;  // the all-zero tile after the kept ones (bf16 pack writes it), or null
   int* err;
 };
 
@@ -98,8 +100,8 @@ cudaError_t launch_stats_bf16(const CompressParams& p, const CUtensorMap& tq,
                               const CUtensorMap& tk, cudaStream_t s);
 cudaError_t launch_stats_f32(const CompressParams& p, const float* q, const float* k,
                              cudaStream_t s);
+// Selection and, in its last CTA, the row_ptr scan.
 cudaError_t launch_select(const CompressParams& p, cudaStream_t s);
-cudaError_t launch_scan(const CompressParams& p, cudaStream_t s);
 cudaError_t launch_pack_bf16(const CompressParams& p, const CUtensorMap& tq,
                              const CUtensorMap& tk, const CUtensorMap& tvals,
                              cudaStream_t s);

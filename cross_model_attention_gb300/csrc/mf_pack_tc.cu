@@ -129,6 +129,11 @@ __global__ void __launch_bounds__(kPackThreads, (BLK == 64) ? 2 : 1)
     // ------------------------------------------------------------ planner
     int* fl0 = reinterpret_cast<int*>(smem + Lay::kFl);  // position of column bj in kept list 0 (or -1)
     int* fl1 = fl0 + kMaxU;
+    // the all-zero tile the retrieval reads for a head's dropped block
+    if (blockIdx.x == 0 && p.zero_tile) {
+      uint4* z = reinterpret_cast<uint4*>(p.zero_tile);
+      for (int i = lane; i < BLK * BLK / 8; i += 32) z[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
     for (int k = 0;; ++k) {
       if (misc[1]) break;
       if (!warp_wait(barFree(k), ((k >> 1) & 1) ^ 1, p.err)) {

@@ -15,10 +15,11 @@
 // Kernels here:
 //   select_kernel   one warp per BSR row: bitonic sort of the candidates in
 //                   registers, fixed-point prefix sum by warp shuffles, kept
-//                   list ascending by ballots
-//   scan_kernel     row_ptr = exclusive scan of the kept counts (single CTA,
-//                   warp-aggregated: per-thread serial chunk, warp shuffles,
-//                   one shared-memory pass over warp totals)
+//                   list ascending by ballots; every candidate's tile index is
+//                   reset to -1 (the pack kernel fills in the kept ones).  The
+//                   last CTA to finish computes row_ptr = exclusive scan of
+//                   the kept counts (warp-aggregated: per-thread serial chunk,
+//                   warp shuffles, one shared-memory pass over warp totals)
 //   union_kernel    per block-row, the ascending union over sender heads of
 //                   the kept block columns (the retrieval's iteration list)
 //                   and the kept-tile table re-indexed by union position
@@ -50,18 +51,15 @@ __device__ __forceinline__ unsigned long long shfl_up64(unsigned long long v, in
 // fixed-point values in sorted order are prefix-summed with warp shuffles and
 // the kept columns are compacted in ascending order with ballots.
 template <int E>
-__global__ void __launch_bounds__(kSelThreads) select_kernel(const CompressParams p) {
+__device__ __forceinline__ void select_row(const CompressParams& p, int row, int* flag) {
   constexpr int N = 32 * E;
-  __shared__ int flag_s[kSelThreads / 32][N];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = blockIdx.x * (kSelThreads / 32) + warp;  // h * R + rb
-  if (row >= p.H_s * p.R) return;  // warp-uniform; no CTA-wide barrier below
+  const int lane = threadIdx.x & 31;
   const int h = row / p.R, rb = row - h * p.R;
   const RowBlock rbk = p.rbs[rb];
   const int nb = (rbk.L + p.B - 1) / p.B;
   const int n = p.causal ? rbk.bi + 1 : nb;
   const float* mass = p.mass + static_cast<size_t>(h) * p.C + rbk.cand_off;
-  int* flag = flag_s[warp];
+  for (int i = lane; i < n; i += 32) p.tile_of[static_cast<size_t>(rbk.cand_off + i) * p.H_s + h] = -1;
 
   unsigned long long key[E];
 #pragma unroll
@@ -152,9 +150,9 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const CompressParam
   if (lane == 0) p.kcount[row] = cnt;
 }
 
-constexpr int kScanThreads = 1024;
-
-__global__ void __launch_bounds__(kScanThreads) scan_kernel(const CompressParams p) {
+// row_ptr = exclusive scan of the kept counts, by one CTA of kSelThreads.
+__device__ __forceinline__ void scan_counts(const CompressParams& p) {
+  constexpr int kScanThreads = kSelThreads;
   __shared__ long long wsum[kScanThreads / 32];
   __shared__ long long carry_s;
   if (threadIdx.x == 0 && p.pack_ctr) *p.pack_ctr = 0;  // the pack kernel's item counter
@@ -183,13 +181,14 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(const CompressParams
     if (lane == 31) wsum[warp] = incl;
     __syncthreads();
     if (warp == 0) {
-      long long w = wsum[lane];
+      constexpr int kWarps = kScanThreads / 32;
+      long long w = (lane < kWarps) ? wsum[lane] : 0;
 #pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
+      for (int off = 1; off < kWarps; off <<= 1) {
         const long long y = __shfl_up_sync(0xffffffffu, w, off);
         if (lane >= off) w += y;
       }
-      wsum[lane] = w;  // inclusive over warps
+      if (lane < kWarps) wsum[lane] = w;  // inclusive over warps
     }
     __syncthreads();
     long long run = carry_s + (warp > 0 ? wsum[warp - 1] : 0) + (incl - local);
@@ -206,6 +205,25 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(const CompressParams
     p.row_ptr[n] = static_cast<int>(carry_s);
     *p.nnz_out = carry_s;
   }
+}
+
+// Eight BSR rows per CTA (one per warp); the last CTA to finish also scans.
+template <int E>
+__global__ void __launch_bounds__(kSelThreads) select_kernel(const CompressParams p) {
+  constexpr int N = 32 * E;
+  __shared__ int flag_s[kSelThreads / 32][N];
+  const int warp = threadIdx.x >> 5;
+  const int row = blockIdx.x * (kSelThreads / 32) + warp;  // h * R + rb
+  if (row < p.H_s * p.R) select_row<E>(p, row, flag_s[warp]);
+  // the last CTA to finish turns the kept counts into row_ptr
+  __shared__ int last_s;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) last_s = (atomicAdd(p.sel_done, 1) == static_cast<int>(gridDim.x) - 1);
+  __syncthreads();
+  if (!last_s) return;
+  __threadfence();
+  scan_counts(p);
 }
 
 // One CTA per global block-row: union over heads of the kept columns.
@@ -275,11 +293,6 @@ cudaError_t launch_select(const CompressParams& p, cudaStream_t s) {
   else if (p.max_cand <= 128) select_kernel<4><<<grid, kSelThreads, 0, s>>>(p);
   else if (p.max_cand <= 256) select_kernel<8><<<grid, kSelThreads, 0, s>>>(p);
   else return cudaErrorInvalidValue;  // at most 256 blocks per sequence
-  return cudaGetLastError();
-}
-
-cudaError_t launch_scan(const CompressParams& p, cudaStream_t s) {
-  scan_kernel<<<1, kScanThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -171,6 +171,7 @@ __global__ void __launch_bounds__(StatWarps<BLK>::kThreads, 1)
     mbar_init(barDone, 1);
     *stat_fail = 0;
     fence_mbar_init();
+    if (blockIdx.x == 0 && p.sel_done) *p.sel_done = 0;  // the selection kernel's CTA count
   }
   if (warp == 1) tmem_alloc(sb + Lay::kSlot, 512);
   tc_fence_before();

@@ -234,7 +234,8 @@ MF_API int mf_device_status(mf_bsr_t h, void* stream);
 /* ---- per-kernel timing (CUDA events on the launching stream) ------------ */
 #define MF_K_STATS    0   /* compressor statistics (Q.K^T, row stats, masses) */
 #define MF_K_SELECT   1   /* block-level top-p                                */
-#define MF_K_SCAN     2   /* row_ptr scan                                     */
+#define MF_K_SCAN     2   /* row_ptr scan (done by the selection kernel's last
+                             CTA: no launches of its own)                     */
 #define MF_K_PACK     3   /* BSR pack (kept-tile recompute + store)           */
 #define MF_K_UNION    4   /* retrieval plan (union of kept columns)           */
 #define MF_K_RETRIEVE 5   /* fused retrieval                                  */
