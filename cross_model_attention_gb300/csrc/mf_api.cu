@@ -100,6 +100,7 @@ struct LayerState {
   int* union_cnt = nullptr;
   int* union_list = nullptr;
   int* utile = nullptr;
+  uint32_t* umask = nullptr;
   long long* nnz_dev = nullptr;
   int* col_idx = nullptr;
   uint16_t* values = nullptr;
@@ -370,6 +371,7 @@ int mf_compress(mf_bsr_t h, int layer, const void* q, const void* k, int dtype, 
   const size_t o_uc = off; off += align_up((size_t)h->R * 4);
   const size_t o_ul = off; off += align_up((size_t)h->C * 4);
   const size_t o_ut = off; off += align_up(HC * 4);
+  const size_t o_um = off; off += align_up((size_t)h->R * 8 * 4);
   const size_t o_nnz = off; off += 256;
   L.meta = dev_alloc(h, off, s);
   if (!L.meta) return fail(MF_ERR_OOM, "allocation of %zu bytes failed", off);
@@ -385,6 +387,7 @@ int mf_compress(mf_bsr_t h, int layer, const void* q, const void* k, int dtype, 
   L.union_cnt = (int*)(mb + o_uc);
   L.union_list = (int*)(mb + o_ul);
   L.utile = (int*)(mb + o_ut);
+  L.umask = (uint32_t*)(mb + o_um);
   L.nnz_dev = (long long*)(mb + o_nnz);
 
   CompressParams cp{};
@@ -412,6 +415,7 @@ int mf_compress(mf_bsr_t h, int layer, const void* q, const void* k, int dtype, 
   cp.union_cnt = L.union_cnt;
   cp.union_list = L.union_list;
   cp.utile = L.utile;
+  cp.umask = (dtype == MF_DTYPE_BF16) ? L.umask : nullptr;  // zeroed by the bf16 statistics kernel
   cp.nnz_out = L.nnz_dev;
   cp.pack_ctr = reinterpret_cast<int*>(L.nnz_dev + 1);  // in the 256-byte scalar slot
   cp.sel_done = reinterpret_cast<int*>(L.nnz_dev + 1) + 1;
@@ -476,6 +480,9 @@ int mf_compress(mf_bsr_t h, int layer, const void* q, const void* k, int dtype, 
             "zero tile");
   else
     cp.zero_tile = reinterpret_cast<uint16_t*>(reinterpret_cast<char*>(L.values) + L.values_bytes);
+  // the bf16 pack kernel writes the retrieval's union tables from the
+  // selection's masks
+  cp.union_in_pack = (dtype == MF_DTYPE_BF16 && cap > 0) ? 1 : 0;
   if (cap > 0) {
     if (dtype == MF_DTYPE_BF16) {
       CUtensorMap tvals{};
@@ -491,7 +498,8 @@ int mf_compress(mf_bsr_t h, int layer, const void* q, const void* k, int dtype, 
               "pack kernel (fp32)");
     }
   }
-  MF_CUDA(timed(h, MF_K_UNION, s, [&] { return launch_union(cp, s); }), "union kernel");
+  if (!cp.union_in_pack)
+    MF_CUDA(timed(h, MF_K_UNION, s, [&] { return launch_union(cp, s); }), "union kernel");
   if ((rc = make_map(&L.pmap, L.values, B, (uint64_t)(cap + 1) * B, (uint64_t)B * 2, 64, 64)) != MF_OK)
     return rc;
   L.valid = true;

@@ -20,8 +20,9 @@
 // never wait on one another), warp 10 plans the next item while the
 // current one runs: the ascending union of its block-rows' kept columns, the
 // rows' statistics, and the col_idx / per-(block, head) tile index entries
-// used by the retrieval.  Plans are double-buffered, so item setup is off
-// the critical path.
+// used by the retrieval, with this head's column of the retrieval's
+// union-ordered tile table (and, for head 0, the union list).  Plans are
+// double-buffered, so item setup is off the critical path.
 #include <cmath>
 
 #include "mf_internal.cuh"
@@ -206,6 +207,38 @@ __global__ void __launch_bounds__(kPackThreads, (BLK == 64) ? 2 : 1)
       }
       // exponent offset of each row: m_i log2(e) + log2(l_i), so that the
       // division by the row sum folds into the exp2
+      // the retrieval's tables, from the selection's union masks: this
+      // head's tile index at every union column of the block-row (-1 where it
+      // dropped the block) and, for head 0, the union list itself
+      if (p.union_in_pack) {
+        for (int t = 0; t < 2; ++t) {
+          if (rbv[t] < 0) continue;
+          const RowBlock rbk = p.rbs[rbv[t]];
+          const int ncand = p.causal ? rbk.bi + 1 : (rbk.L + BLK - 1) / BLK;
+          const uint32_t mw = (lane < 8) ? p.umask[rbv[t] * 8 + lane] : 0u;
+          int pre = __popc(mw);
+#pragma unroll
+          for (int off = 1; off < 8; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, pre, off);
+            if (lane >= off) pre += y;
+          }
+          const int ucnt = __shfl_sync(0xffffffffu, pre, 7);
+          pre -= __popc(mw);  // exclusive over the words
+          const int* flt = t ? fl1 : fl0;
+          for (int c0 = 0; c0 < ncand; c0 += 32) {
+            const uint32_t word = __shfl_sync(0xffffffffu, mw, c0 >> 5);
+            const int wpre = __shfl_sync(0xffffffffu, pre, c0 >> 5);
+            const int bj = c0 + lane;
+            if (bj < ncand && ((word >> lane) & 1u)) {
+              const int j = wpre + __popc(word & ((1u << lane) - 1u));
+              const int pos = flt[bj];
+              p.utile[static_cast<size_t>(rbk.cand_off + j) * p.H_s + h] = pos >= 0 ? base[t] + pos : -1;
+              if (h == 0) p.union_list[rbk.cand_off + j] = bj;
+            }
+          }
+          if (h == 0 && lane == 0) p.union_cnt[rbv[t]] = ucnt;
+        }
+      }
       float* m2 = reinterpret_cast<float*>(pl + kPlM2);
       for (int r = lane; r < kRows; r += 32) {
         const int row_local = tile.tl * kRows + r;

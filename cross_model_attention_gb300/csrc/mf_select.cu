@@ -15,8 +15,9 @@
 // Kernels here:
 //   select_kernel   one warp per BSR row: bitonic sort of the candidates in
 //                   registers, fixed-point prefix sum by warp shuffles, kept
-//                   list ascending by ballots; every candidate's tile index is
-//                   reset to -1 (the pack kernel fills in the kept ones).  The
+//                   list ascending by ballots, OR-ed into the block-row's
+//                   union mask; every candidate's tile index is reset to -1
+//                   (the pack kernel fills in the kept ones).  The
 //                   last CTA to finish computes row_ptr = exclusive scan of
 //                   the kept counts (warp-aggregated: per-thread serial chunk,
 //                   warp shuffles, one shared-memory pass over warp totals)
@@ -145,6 +146,8 @@ __device__ __forceinline__ void select_row(const CompressParams& p, int row, int
     const bool f = (bj < n) && flag[bj];
     const uint32_t m = __ballot_sync(0xffffffffu, f);
     if (f) out[cnt + __popc(m & ((1u << lane) - 1u))] = bj;
+    // the block-row's union over heads, as a bit mask of 8 words
+    if (lane == 0 && m != 0u && p.umask) atomicOr(&p.umask[rb * 8 + (c0 >> 5)], m);
     cnt += __popc(m);
   }
   if (lane == 0) p.kcount[row] = cnt;
