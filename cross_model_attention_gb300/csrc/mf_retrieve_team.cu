@@ -33,7 +33,8 @@
 //     64 keys) and V_c and accumulates O[(head, row), d] += A_hat . V_c on
 //     tcgen05 (two heads x 64 rows per M = 128 tile, N = d) into TMEM over the
 //     slab's blocks, then bumps the slot's freed counter.
-// The ring (6 slots per team) lives in L2 between its write and its reads;
+// The ring (8 slots per team) lives in L2 between its write and its reads
+// (the sender tiles are copied with an evict-first L2 policy);
 // every sender-tile byte is read from HBM once.  Slabs go to teams heaviest
 // first onto the least-loaded team (a host-side table); within a team all
 // CTAs walk the same slab list,
@@ -59,7 +60,7 @@ constexpr int kPBytes = 96 * 1024;  // P ring: whole blocks of 16-head slices (8
 constexpr int kSliceBytes = 8 * 16 * 128;
 constexpr int kPBMax = 3;       // block slots of the P ring at most
 constexpr int kNComb = 32;      // combine N: 8 groups x 4 head slots
-constexpr int kRing = 6;        // global ring slots per team
+constexpr int kRing = 8;        // global ring slots per team
 constexpr int kASlots = 2;      // A_hat^T tiles staged in shared memory
 constexpr int kSlotHeads = 4;   // head slots per group
 constexpr int kIdxSlots = 8;    // tile-index ring of the copy warps (blocks)
@@ -331,6 +332,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         const int* irow = idx_ring + (u % kIdxSlots) * 64;
+        // sender tiles are read once: evicted from L2 before the exchange ring
+        const uint64_t pol = policy_evict_first();
         int tix[4];
 #pragma unroll
         for (int sl = 0; sl < 4; ++sl) {
@@ -357,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t nbytes = tt >= 0 ? 16u : 0u;  // a dropped head is zero-filled
           const uint32_t dst = dst0 + (pb * lay.nslice + sl) * kSliceBytes;
 #pragma unroll
-          for (int rr = 0; rr < 8; ++rr) cp_async16(dst + rr * 2048, src + rr * row_bytes, nbytes);
+          for (int rr = 0; rr < 8; ++rr) cp_async16_hint(dst + rr * 2048, src + rr * row_bytes, nbytes, pol);
         }
         cp_async_arrive(bar(kBarPFull + pb));
       }

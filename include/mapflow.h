@@ -177,7 +177,7 @@ MF_API int mf_compress(mf_bsr_t h, int layer, const void* q, const void* k, int 
  * Rows of blocks with no kept tile get O = 0.  Asynchronous.
  * With 8 KV heads and H_r <= 32 (bf16) the kernel is a cooperative launch
  * whose CTAs pass partial results through a small exchange ring owned by the
- * handle (about 30 MB, allocated with the handle's allocator on the first such
+ * handle (about 40 MB, allocated with the handle's allocator on the first such
  * call, on `stream`): calls of one handle must therefore not run concurrently
  * on different streams.
  * Errors: MF_ERR_ARG, MF_ERR_UNSUPPORTED, MF_ERR_STATE, MF_ERR_CUDA, MF_ERR_OOM.
