@@ -427,10 +427,20 @@ int mf_compress(mf_bsr_t h, int layer, const void* q, const void* k, int dtype, 
     if ((reinterpret_cast<uintptr_t>(q) & 15) || (reinterpret_cast<uintptr_t>(k) & 15))
       return fail(MF_ERR_ARG, "q and k must be 16-byte aligned");
     if ((rc = make_map(&tq, q, (uint64_t)H_s * d, T, (uint64_t)H_s * d * 2, 64, 128)) != MF_OK) return rc;
-    if ((rc = make_map(&tk, k, (uint64_t)H_ks * d, T, (uint64_t)H_ks * d * 2, 64, 128)) != MF_OK) return rc;
     if ((rc = make_map(&tk_pack, k, (uint64_t)H_ks * d, T, (uint64_t)H_ks * d * 2, 64, B)) != MF_OK) return rc;
-    MF_CUDA(timed(h, MF_K_STATS, s, [&] { return launch_stats_bf16(cp, tq, tk, s); }),
-            "statistics kernel");
+    if (stats2_supported(h->max_cand)) {
+      // two CTAs per SM on 64-key tiles (rows of at most 128 candidate blocks)
+      CUtensorMap tk64 = tk_pack;
+      if (B != 64 &&
+          (rc = make_map(&tk64, k, (uint64_t)H_ks * d, T, (uint64_t)H_ks * d * 2, 64, 64)) != MF_OK)
+        return rc;
+      MF_CUDA(timed(h, MF_K_STATS, s, [&] { return launch_stats2_bf16(cp, tq, tk64, s); }),
+              "statistics kernel");
+    } else {
+      if ((rc = make_map(&tk, k, (uint64_t)H_ks * d, T, (uint64_t)H_ks * d * 2, 64, 128)) != MF_OK) return rc;
+      MF_CUDA(timed(h, MF_K_STATS, s, [&] { return launch_stats_bf16(cp, tq, tk, s); }),
+              "statistics kernel");
+    }
   } else {
     MF_CUDA(timed(h, MF_K_STATS, s,
                   [&] { return launch_stats_f32(cp, (const float*)q, (const float*)k, s); }),

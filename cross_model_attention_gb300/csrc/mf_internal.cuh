@@ -98,6 +98,11 @@ inline cudaError_t sm_count(int* out) {
 
 // -------------------------------------------------------------- launchers --
 // All return cudaError_t of the launch (cudaSuccess when enqueued).
+// Statistics with two CTAs per SM (64-key S tiles) for rows of at most 128
+// candidate blocks; tk64 boxes are 64 keys high.
+bool stats2_supported(int max_cand);
+cudaError_t launch_stats2_bf16(const CompressParams& p, const CUtensorMap& tq,
+                               const CUtensorMap& tk64, cudaStream_t s);
 cudaError_t launch_stats_bf16(const CompressParams& p, const CUtensorMap& tq,
                               const CUtensorMap& tk, cudaStream_t s);
 cudaError_t launch_stats_f32(const CompressParams& p, const float* q, const float* k,
