@@ -98,11 +98,14 @@ def pack_bytes(w, nnz: int) -> float:
                  + 4 * nnz)
 
 
-def traffic_for(kernel: str):
+def traffic_for(kernel: str, max_blocks: int = 0):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current source of that kernel; else None."""
+    on the current source of that kernel; else None.  The statistics step
+    runs the two-CTAs-per-SM kernel when no row has more than 128 candidate
+    blocks (`max_blocks`), the one-CTA kernel otherwise."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
-    src = {"stats": "mf_stats_tc.cu", "pack": "mf_pack_tc.cu", "retrieve": "mf_retrieve_team.cu"}[kernel]
+    stats_src = "mf_stats2_tc.cu" if max_blocks <= 128 else "mf_stats_tc.cu"
+    src = {"stats": stats_src, "pack": "mf_pack_tc.cu", "retrieve": "mf_retrieve_team.cu"}[kernel]
     with open(os.path.join(ROOT, "cross_model_attention_gb300", "csrc", src), "rb") as fh:
         sha = hashlib.sha256(fh.read()).hexdigest()[:16]
     if not os.path.exists(path):
@@ -357,6 +360,8 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
     tf_sus = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
     label = "of measured" if src == "measured" else "of fallback"
 
+    max_blocks = max(-(-L // w.B) for L in w.seqlens)  # candidate blocks of the longest row
+
     def roof(kind):
         n, ms = prof[kind]
         if kind == "retrieve":  # bracketed by the step events (launch gaps included)
@@ -365,7 +370,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
         if kind == "stats":
             ach = comp_flops / Ls / per / 1e12
             return {"bound": "tensor", "achieved": ach, "peak": tf_sus, "unit": "TFLOP/s",
-                    "frac": ach / tf_sus, "traffic": traffic_for("stats"), "launches": n,
+                    "frac": ach / tf_sus, "traffic": traffic_for("stats", max_blocks), "launches": n,
                     "ms_per_launch": per * 1e3, "peak_source": f"bf16_tflops_sustained ({label})"}
         if kind == "pack":
             ach = pk_bytes / Ls / per / 1e9

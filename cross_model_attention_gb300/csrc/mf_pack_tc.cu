@@ -450,7 +450,8 @@ __global__ void __launch_bounds__(kPackThreads, (BLK == 64) ? 2 : 1)
         fence_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_store_2d(&tvals, wstg, c_base, (base_sub + pos) * BLK + rloc0);
+          // the tiles are read by the retrieval, long after: evict them first
+          tma_store_2d_hint(&tvals, wstg, c_base, (base_sub + pos) * BLK + rloc0, policy_evict_first());
           bulk_commit();
         }
       }

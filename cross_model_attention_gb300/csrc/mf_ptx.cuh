@@ -69,6 +69,12 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* er
   }
 }
 
+// L2 policy for data read once (streamed): its lines are evicted first.
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
 // -------------------------------------------------------------------- TMA --
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
                                             uint32_t bar) {
@@ -82,6 +88,16 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t sr
   asm volatile(
       "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(map),
       "r"(src), "r"(x), "r"(y)
+      : "memory");
+}
+// TMA tensor store with an L2 cache policy (e.g. evict-first for output that
+// is not read again by this kernel).
+__device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap* map, uint32_t src, int x, int y,
+                                                  uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3}], [%1], %4;" ::"l"(
+          map),
+      "r"(src), "r"(x), "r"(y), "l"(pol)
       : "memory");
 }
 __device__ __forceinline__ void bulk_commit() {
@@ -243,12 +259,6 @@ __device__ __forceinline__ void prefetch_l2(const void* ptr, uint32_t bytes) {
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
                : "memory");
-}
-// L2 policy for data read once (streamed): its lines are evicted first.
-__device__ __forceinline__ uint64_t policy_evict_first() {
-  uint64_t pol;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-  return pol;
 }
 // 16-byte asynchronous copy with an L2 cache policy.
 __device__ __forceinline__ void cp_async16_hint(uint32_t dst, const void* src, uint32_t src_bytes,
