@@ -117,6 +117,25 @@ def traffic_for(kernel: str, max_blocks: int = 0):
     return None
 
 
+def link_bandwidth(host, dev, stream, reps=8):
+    """Host<->device copy bandwidth (GB/s) of one pinned buffer, measured
+    right after the end-to-end leg: the host link is shared with other jobs
+    on the machine and varies from run to run."""
+    import torch
+    out = {}
+    for name, f in (("h2d", lambda: dev.copy_(host, non_blocking=True)),
+                    ("d2h", lambda: host.copy_(dev, non_blocking=True))):
+        f()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            f()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        out[name] = round(reps * host.numel() * host.element_size() / (e0.elapsed_time(e1) / 1e3) / 1e9, 1)
+    return out
+
+
 # -------------------------------------------------------------- clocks ----
 
 class ClockSampler:
@@ -432,7 +451,8 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
         h2d = (q_h.numel() + k_h.numel() + v_h.numel()) * 2 + W_h.numel() * 4
         e2e = {"value": ret_bytes * reps * world / tr / 1e9, "unit": "GB/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(o_h.numel() * 2 + 16 * Ls),
-               "compressor_tokens_per_s": T * Ls * reps * world / tc}
+               "compressor_tokens_per_s": T * Ls * reps * world / tc,
+               "link_gbs": link_bandwidth(q_h[0], q_d[0], stream)}
 
     bsr.close()
     out = None
