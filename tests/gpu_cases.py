@@ -88,7 +88,9 @@ def check_block_rows(ex, q64, k64, grid: orc.BlockGrid, H_s: int, pairs: Iterabl
         bad = err > MASS_RTOL * np.abs(ref["mass"]) + 1e-30
         assert not bad.any(), f"mass (h={h}, rb={rb}) rel err {np.max(err / np.abs(ref['mass']))}"
         rows = ref["rows"]
-        assert np.abs(rmax[h, rows] - ref["m"]).max() < 1e-5, "row max differs"
+        # m_i in fp32 carries three roundings (score, scale to log2 units,
+        # back to natural units): 1e-5 absolute plus 1e-6 relative
+        assert (np.abs(rmax[h, rows] - ref["m"]) <= 1e-5 + 1e-6 * np.abs(ref["m"])).all(), "row max differs"
         assert (np.abs(rsum[h, rows] - ref["l"]) <= 1e-5 * ref["l"]).all(), "row sum differs"
         r = h * grid.R + rb
         B = grid.B

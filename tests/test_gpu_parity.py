@@ -103,6 +103,61 @@ def test_unstructured_random_logits():
     small_case((448,), 3, 3, 128, 64, 0.9, 6, 3, structured=False, seed=7)
 
 
+def test_extreme_logits():
+    """Scores far outside the usual range: a row's first key block sits near
+    -90 (natural units, about -130 in log2 units) and, for rows past it, the
+    next block near +90, so the statistics kernels must take a row's first
+    block against its own max and later re-reference across a gap no sum of
+    exp2 terms could span.  Every product and sum of q.k is an exact fp32
+    integer (one large dimension, one of small integers), so the oracle's
+    fp64 scores are the kernel's scores."""
+    T, Hs, d, B, p = 384, 2, 64, 64, 0.9
+    rng = np.random.default_rng(11)
+    q = np.zeros((T, Hs, d), np.float32)
+    k = np.zeros((T, Hs, d), np.float32)
+    q[:, :, 0] = 8.0
+    q[:, :, 1] = 1.0
+    k[:64, :, 0] = -90.0
+    k[64:128, :, 0] = 90.0
+    k[:, :, 1] = rng.integers(-8, 9, size=(T, Hs)).astype(np.float32)
+    qb, kb = synth.bf16_round(q), synth.bf16_round(k)
+    x = {"q": qb, "k": kb, "q64": synth.bf16_to_f64(qb), "k64": synth.bf16_to_f64(kb)}
+    cu = np.array([0, T], np.int32)
+    bsr = mapflow.BSR(1, T, Hs, B, cu)
+    gc.run_compress(bsr, 0, x, "bf16", p)
+    ex = gc.export_np(bsr, 0)
+    grid = orc.BlockGrid(cu, B, True)
+    gc.check_structure(ex, grid, Hs, p)
+    gc.check_block_rows(ex, x["q64"], x["k64"], grid, Hs, [(h, rb) for h in range(Hs) for rb in range(grid.R)])
+    v = synth.random_v(T, 2, d, 5)
+    W = synth.random_w(4, Hs, 6)
+    O = gc.run_retrieve(bsr, W[None], v["v"][None], 4, "bf16", [0])
+    gc.check_output(O[0], x["q64"], x["k64"], grid, ex, Hs, W, v["v64"], 2, range(grid.R))
+    bsr.close()
+
+
+@pytest.mark.parametrize("L", [8192, 8193])
+def test_statistics_kernel_boundary(L):
+    """8192 tokens at B = 64 give rows of 128 candidate blocks (the statistics
+    kernel with two CTAs per SM); 8193 give 129 (the one-CTA kernel).  Sampled
+    block-rows, the full selection and the retrieval against the oracle."""
+    Hs, d, B, p = 2, 64, 64, 0.95
+    x = synth.random_qk(L, Hs, Hs, d, 3)
+    cu = np.array([0, L], np.int32)
+    bsr = mapflow.BSR(1, L, Hs, B, cu)
+    gc.run_compress(bsr, 0, x, "bf16", p)
+    ex = gc.export_np(bsr, 0)
+    grid = orc.BlockGrid(cu, B, True)
+    gc.check_structure(ex, grid, Hs, p)
+    rows = [0, 1, grid.R // 2, grid.R - 2, grid.R - 1]
+    gc.check_block_rows(ex, x["q64"], x["k64"], grid, Hs, [(h, rb) for h in range(Hs) for rb in rows])
+    v = synth.random_v(L, 8, d, 4)
+    W = synth.random_w(16, Hs, 5)
+    O = gc.run_retrieve(bsr, W[None], v["v"][None], 16, "bf16", [0])
+    gc.check_output(O[0], x["q64"], x["k64"], grid, ex, Hs, W, v["v64"], 8, rows)
+    bsr.close()
+
+
 def test_fp32_workload0():
     """The fp32 workload exactly: N=512, H_s=4, d=64, B=64, p=0.95, W = I + N(0,1/4)."""
     w = workloads.get(0)
