@@ -100,7 +100,7 @@ struct LayerState {
   int* union_cnt = nullptr;
   int* union_list = nullptr;
   int* utile = nullptr;
-  uint32_t* umask = nullptr;
+  uint32_t* kmask = nullptr;
   long long* nnz_dev = nullptr;
   int* col_idx = nullptr;
   uint16_t* values = nullptr;
@@ -371,7 +371,7 @@ int mf_compress(mf_bsr_t h, int layer, const void* q, const void* k, int dtype, 
   const size_t o_uc = off; off += align_up((size_t)h->R * 4);
   const size_t o_ul = off; off += align_up((size_t)h->C * 4);
   const size_t o_ut = off; off += align_up(HC * 4);
-  const size_t o_um = off; off += align_up((size_t)h->R * 8 * 4);
+  const size_t o_km = off; off += align_up(HR * 8 * 4);
   const size_t o_nnz = off; off += 256;
   L.meta = dev_alloc(h, off, s);
   if (!L.meta) return fail(MF_ERR_OOM, "allocation of %zu bytes failed", off);
@@ -387,7 +387,7 @@ int mf_compress(mf_bsr_t h, int layer, const void* q, const void* k, int dtype, 
   L.union_cnt = (int*)(mb + o_uc);
   L.union_list = (int*)(mb + o_ul);
   L.utile = (int*)(mb + o_ut);
-  L.umask = (uint32_t*)(mb + o_um);
+  L.kmask = (uint32_t*)(mb + o_km);
   L.nnz_dev = (long long*)(mb + o_nnz);
 
   CompressParams cp{};
@@ -415,7 +415,7 @@ int mf_compress(mf_bsr_t h, int layer, const void* q, const void* k, int dtype, 
   cp.union_cnt = L.union_cnt;
   cp.union_list = L.union_list;
   cp.utile = L.utile;
-  cp.umask = (dtype == MF_DTYPE_BF16) ? L.umask : nullptr;  // zeroed by the bf16 statistics kernel
+  cp.kmask = (dtype == MF_DTYPE_BF16) ? L.kmask : nullptr;
   cp.nnz_out = L.nnz_dev;
   cp.pack_ctr = reinterpret_cast<int*>(L.nnz_dev + 1);  // in the 256-byte scalar slot
   cp.sel_done = reinterpret_cast<int*>(L.nnz_dev + 1) + 1;

@@ -56,7 +56,7 @@ struct CompressParams {
   int* pack_ctr;    // device scalar: the pack kernel's next item (reset by the selection kernel)
   int* sel_done;    // device scalar: selection CTAs finished (reset by the statistics kernel)
   uint16_t* zero_tile;  // the all-zero tile after the kept ones (bf16 pack writes it), or null
-  uint32_t* umask;  // [R][8] union of the kept columns over heads (bf16 path), or null
+  uint32_t* kmask;  // [H_s*R][8] kept columns of each BSR row as bit masks (bf16 path), or null
   int union_in_pack;  // 1: the bf16 pack kernel writes union_cnt / union_list / utile
   int* err;
 };

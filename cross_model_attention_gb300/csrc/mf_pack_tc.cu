@@ -207,23 +207,29 @@ __global__ void __launch_bounds__(kPackThreads, (BLK == 64) ? 2 : 1)
       }
       // exponent offset of each row: m_i log2(e) + log2(l_i), so that the
       // division by the row sum folds into the exp2
-      // the retrieval's tables, from the selection's union masks: this
-      // head's tile index at every union column of the block-row (-1 where it
-      // dropped the block) and, for head 0, the union list itself
+      // the retrieval's tables, from the selection's per-row kept-column
+      // masks: this head's tile index at every union column of the block-row
+      // (-1 where it dropped the block) and, for head 0, the union list
       if (p.union_in_pack) {
         for (int t = 0; t < 2; ++t) {
           if (rbv[t] < 0) continue;
           const RowBlock rbk = p.rbs[rbv[t]];
           const int ncand = p.causal ? rbk.bi + 1 : (rbk.L + BLK - 1) / BLK;
-          const uint32_t mw = (lane < 8) ? p.umask[rbv[t] * 8 + lane] : 0u;
-          int pre = __popc(mw);
+          // union over the heads of their kept-column masks: lane w + 8j ORs
+          // word w of heads j, j + 4, ...; then the four partial ORs combine
+          uint32_t mw = 0u;
+          for (int hh = lane >> 3; hh < p.H_s; hh += 4)
+            mw |= p.kmask[(static_cast<size_t>(hh) * p.R + rbv[t]) * 8 + (lane & 7)];
+          mw |= __shfl_xor_sync(0xffffffffu, mw, 8);
+          mw |= __shfl_xor_sync(0xffffffffu, mw, 16);
+          int pre = (lane < 8) ? __popc(mw) : 0;
 #pragma unroll
           for (int off = 1; off < 8; off <<= 1) {
             const int y = __shfl_up_sync(0xffffffffu, pre, off);
             if (lane >= off) pre += y;
           }
           const int ucnt = __shfl_sync(0xffffffffu, pre, 7);
-          pre -= __popc(mw);  // exclusive over the words
+          pre -= (lane < 8) ? __popc(mw) : 0;  // exclusive over the words
           const int* flt = t ? fl1 : fl0;
           for (int c0 = 0; c0 < ncand; c0 += 32) {
             const uint32_t word = __shfl_sync(0xffffffffu, mw, c0 >> 5);

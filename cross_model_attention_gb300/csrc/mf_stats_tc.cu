@@ -132,10 +132,6 @@ __global__ void __launch_bounds__(StatWarps<BLK>::kThreads, 1)
     fence_mbar_init();
     if (blockIdx.x == 0 && p.sel_done) *p.sel_done = 0;  // the selection kernel's CTA count
   }
-  // the selection kernel ORs each head's kept columns into these masks
-  if (p.umask)
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < p.R * 8; i += gridDim.x * blockDim.x)
-      p.umask[i] = 0u;
   if (warp == 1) tmem_alloc(sb + Lay::kSlot, 512);
   tc_fence_before();
   __syncthreads();
