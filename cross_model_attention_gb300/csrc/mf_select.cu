@@ -15,8 +15,8 @@
 // Kernels here:
 //   select_kernel   one warp per BSR row: bitonic sort of the candidates in
 //                   registers, fixed-point prefix sum by warp shuffles, kept
-//                   list ascending by ballots, OR-ed into the block-row's
-//                   union mask; every candidate's tile index is reset to -1
+//                   list ascending by ballots and as an 8-word bit mask of
+//                   the row; every candidate's tile index is reset to -1
 //                   (the pack kernel fills in the kept ones).  The
 //                   last CTA to finish computes row_ptr = exclusive scan of
 //                   the kept counts (warp-aggregated: per-thread serial chunk,
