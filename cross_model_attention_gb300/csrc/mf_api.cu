@@ -581,6 +581,8 @@ int mf_retrieve(mf_bsr_t h, const float* W, const void* v, void* o, int dtype, i
           h->ring = dev_alloc(h, retrieve_team_ring_bytes(cap), s);
           h->ring_flags = (uint32_t*)dev_alloc(h, retrieve_team_flag_bytes(cap), s);
           if (!h->ring || !h->ring_flags) return fail(MF_ERR_OOM, "exchange ring allocation failed");
+          // zero once: each launch leaves the counters at zero when it ends
+          MF_CUDA(cudaMemsetAsync(h->ring_flags, 0, retrieve_team_flag_bytes(cap), s), "ring reset");
           h->ring_teams = cap;
         }
         if (h->team_slab_teams != teams) {
@@ -617,7 +619,6 @@ int mf_retrieve(mf_bsr_t h, const float* W, const void* v, void* o, int dtype, i
         rc = make_map(&ta, h->ring, 64, (uint64_t)retrieve_team_ring_rows(h->ring_teams), 128, 64,
                       (uint32_t)retrieve_team_ring_box_rows(H_r));
         if (rc != MF_OK) return rc;
-        MF_CUDA(cudaMemsetAsync(h->ring_flags, 0, retrieve_team_flag_bytes(teams), s), "ring reset");
         MF_CUDA(timed(h, MF_K_RETRIEVE, s,
                       [&] {
                         return launch_retrieve_team(rp, ta, tv, ox, h->ring, h->ring_flags, teams, s);

@@ -120,7 +120,8 @@ cudaError_t launch_retrieve_bf16(const RetrieveParams& p, const CUtensorMap& tp,
 // Team retrieval: persistent cooperative kernel, teams of 8 CTAs exchanging
 // the combined maps through a ring in global memory (`ring` of
 // retrieve_team_ring_bytes, `flags` of retrieve_team_flag_bytes, zeroed
-// before every launch; `ta` maps the ring as retrieve_team_ring_rows x 64 bf16
+// once: every launch leaves them at zero; `ta` maps the ring as
+// retrieve_team_ring_rows x 64 bf16
 // with boxes of 64 x retrieve_team_ring_box_rows).
 bool retrieve_team_supported(int H_s, int H_r, int H_kv, int d, int B);
 int retrieve_team_count(int n_slabs, int sms);

@@ -191,8 +191,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int hpc = p.H_r / kTeam;
   const TeamLayout lay(D, p.H_s, hpc);
   constexpr int kSub = BLK / 64;
-  uint32_t* const ready = flags + team * 2 * kRing;
+  uint32_t* const ready = flags + team * (2 * kRing + 1);
   uint32_t* const freed = ready + kRing;
+  uint32_t* const done = ready + 2 * kRing;  // CTAs of the team that have finished
   const size_t slot_elems = static_cast<size_t>(kTeam) * kGroupElems;
   __nv_bfloat16* ring_team = ring + static_cast<size_t>(team) * kRing * slot_elems;
   auto bar = [&](int i) { return sb + lay.off_bar + 8u * i; };
@@ -583,6 +584,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+  // The team's last CTA to finish (every wait above is bounded, so all get
+  // here) leaves the team's counters at zero for the next launch.
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(done, 1u) == static_cast<uint32_t>(kTeam - 1)) {
+      for (int i = 0; i < 2 * kRing; ++i) ready[i] = 0u;  // ready, then freed
+      *done = 0u;
+      __threadfence();
+    }
+  }
 }
 
 template <int D, int BLK>
@@ -624,7 +635,7 @@ size_t retrieve_team_ring_bytes(int n_teams) {
 }
 
 size_t retrieve_team_flag_bytes(int n_teams) {
-  return static_cast<size_t>(n_teams) * 2 * kRing * sizeof(uint32_t);
+  return static_cast<size_t>(n_teams) * (2 * kRing + 1) * sizeof(uint32_t);
 }
 
 int retrieve_team_ring_box_rows(int) { return kGroupElems / 64; }
