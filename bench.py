@@ -42,6 +42,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from cross_model_attention_gb300 import synth, workloads  # noqa: E402
+from cross_model_attention_gb300.accounting import (  # noqa: E402
+    candidate_blocks, pack_bytes, qk_flops, retrieval_bytes, union_blocks)
 
 METRIC = "retrieval GB/s & % HBM roofline; compressor tokens/s & % tensor peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -76,26 +78,6 @@ def load_peaks():
             pk = json.load(fh)
         return pk, "measured"
     return dict(FALLBACK_PEAKS), "fallback"
-
-
-def qk_flops(w) -> float:
-    """Q.K^T flops of one causal pass over one sender layer."""
-    return float(sum(2.0 * w.d * w.sender_heads * L * (L + 1) / 2 for L in w.seqlens))
-
-
-def retrieval_bytes(w, rcv, nnz: int) -> float:
-    """Algorithmic HBM bytes of one retrieval launch (one reuse layer)."""
-    R = sum((L + w.B - 1) // w.B for L in w.seqlens)
-    return float(nnz * 2 * w.B * w.B + 4 * nnz + 4 * (w.sender_heads * R + 1)
-                 + 4 * rcv.heads * w.sender_heads + 2 * w.T * rcv.kv_heads * w.d
-                 + 2 * w.T * rcv.heads * w.d)
-
-
-def pack_bytes(w, nnz: int) -> float:
-    """Algorithmic HBM bytes of one pack launch: Q and K read once, kept tiles
-    and col_idx written."""
-    return float(2 * w.T * (w.sender_heads + w.sender_kv_heads) * w.d + nnz * 2 * w.B * w.B
-                 + 4 * nnz)
 
 
 def traffic_for(kernel: str, max_blocks: int = 0):
@@ -337,6 +319,13 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
     bsr.device_status()
     nnz = [bsr.info(l)[0] for l in range(Ls)]
     ret_bytes = sum(retrieval_bytes(w, rcv, nnz[m]) for m in layer_map)
+    # tensor work of the retrieval: A_hat.V over each block-row's union of
+    # kept blocks, and the head combine of every kept tile
+    R = sum((L + w.B - 1) // w.B for L in w.seqlens)
+    U = {m: union_blocks(*bsr.structure(m), Hs, R) for m in set(layer_map)}
+    ret_flops = sum(2.0 * w.B * w.B * d * U[m] * rcv.heads + 2.0 * w.B * w.B * rcv.heads * nnz[m]
+                    for m in layer_map)
+    exps = float(sum(L * (L + 1) // 2 for L in w.seqlens)) * Hs  # one exp2 per causal logit
     comp_flops = qk_flops(w) * Ls
     pk_bytes = sum(pack_bytes(w, n) for n in nnz)
 
@@ -473,12 +462,15 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
             "compressor": {"tokens_per_s": comp_tps,
                            "qk_tensor_frac": rooflines["stats"]["frac"],
                            "qk_tflops": rooflines["stats"]["achieved"],
+                           "exp2_per_s": exps * Ls * K * world / t_comp,
+                           "pack_bytes_written_per_step": float(sum(n * (2 * w.B * w.B + 4) for n in nnz)),
                            "ms_per_step": 1e3 * t_comp / K},
             "retrieval": {"ms_per_step": 1e3 * t_ret / K, "bytes_per_step": ret_bytes,
                           "hbm_frac": rooflines["retrieve"]["frac"],
-                          "kept_fraction": float(np.mean(nnz)) / (Hs * sum(
-                              (L + w.B - 1) // w.B * ((L + w.B - 1) // w.B + 1) // 2
-                              for L in w.seqlens))},
+                          "tensor_flops_per_step": ret_flops,
+                          "tensor_frac": ret_flops * K / t_ret / (tf_sus * 1e12),
+                          "binds": "hbm" if rooflines["retrieve"]["frac"] >= ret_flops * K / t_ret / (tf_sus * 1e12) else "tensor",
+                          "kept_fraction": float(np.mean(nnz)) / (Hs * candidate_blocks(w))},
             "roofline": rooflines[dominant] | {"kernel": dominant},
             "rooflines": rooflines,
             "gpu_launches": launches,

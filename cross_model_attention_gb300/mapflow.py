@@ -263,6 +263,17 @@ class BSR:
                     out["row_sum"], stream)
         return out
 
+    def structure(self, layer: int):
+        """(row_ptr, col_idx) of a compressed layer as host numpy arrays."""
+        import torch
+        nnz, n_rows, _ = self.info(layer)
+        dev = torch.device("cuda", torch.cuda.current_device())
+        rp = torch.empty(n_rows + 1, dtype=torch.int32, device=dev)
+        ci = torch.empty(max(nnz, 1), dtype=torch.int32, device=dev)
+        mf_bsr_copy(self.handle, layer, rp, ci if nnz else None, None, None, None, None, None)
+        torch.cuda.synchronize()
+        return rp.cpu().numpy(), ci[:nnz].cpu().numpy().astype(np.int64)
+
     def release_layer(self, layer: int) -> None:
         mf_bsr_release_layer(self.handle, layer)
 
