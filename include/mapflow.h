@@ -237,7 +237,8 @@ MF_API int mf_device_status(mf_bsr_t h, void* stream);
 #define MF_K_SCAN     2   /* row_ptr scan (done by the selection kernel's last
                              CTA: no launches of its own)                     */
 #define MF_K_PACK     3   /* BSR pack (kept-tile recompute + store)           */
-#define MF_K_UNION    4   /* retrieval plan (union of kept columns)           */
+#define MF_K_UNION    4   /* retrieval plan (union of kept columns); on the
+                             bf16 path the pack kernel writes it: no launches */
 #define MF_K_RETRIEVE 5   /* fused retrieval                                  */
 #define MF_K_COUNT    6
 
