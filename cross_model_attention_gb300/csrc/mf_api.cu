@@ -106,6 +106,14 @@ struct LayerState {
   uint16_t* values = nullptr;
   size_t values_bytes = 0, colidx_bytes = 0;
   CUtensorMap pmap;  // values as [(nnz+1)*B rows][B cols], 64x64 boxes (per-group retrieval)
+  // while offloaded: the layer's arrays in pinned host memory owned by the
+  // handle (meta whole, the nnz kept tiles, col_idx); device pointers null
+  bool offloaded = false;
+  void* h_meta = nullptr;
+  void* h_values = nullptr;
+  void* h_colidx = nullptr;
+  size_t h_values_cap = 0, h_colidx_cap = 0;  // allocated host bytes
+  cudaEvent_t ready = nullptr;  // end of the last offload's or prefetch's copies
 };
 
 struct ProfRec {
@@ -168,10 +176,68 @@ void release_layer(mf_bsr_t h, LayerState& L, cudaStream_t s) {
   dev_free(h, L.meta, s);
   dev_free(h, L.values, s);
   dev_free(h, L.col_idx, s);
+  if (L.ready) {
+    cudaEventSynchronize(L.ready);  // no copy may still use the host buffers
+    cudaEventDestroy(L.ready);
+  }
+  if (L.h_meta) cudaFreeHost(L.h_meta);
+  if (L.h_values) cudaFreeHost(L.h_values);
+  if (L.h_colidx) cudaFreeHost(L.h_colidx);
   L = LayerState();
 }
 
 size_t align_up(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Byte offsets of a layer's arrays in its one scratch allocation ("meta").
+struct MetaLayout {
+  size_t mass, max, sum, kc, kept, rp, tile, uc, ul, ut, km, nnz, bytes;
+};
+
+MetaLayout meta_layout(const mf_bsr_s* h) {
+  const size_t HC = (size_t)h->H_s * h->C, HT = (size_t)h->H_s * h->T, HR = (size_t)h->H_s * h->R;
+  MetaLayout m{};
+  size_t off = 0;
+  m.mass = off; off += align_up(HC * 4);
+  m.max = off; off += align_up(HT * 4);
+  m.sum = off; off += align_up(HT * 4);
+  m.kc = off; off += align_up(HR * 4);
+  m.kept = off; off += align_up(HC * 4);
+  m.rp = off; off += align_up((HR + 1) * 4);
+  m.tile = off; off += align_up(HC * 4);
+  m.uc = off; off += align_up((size_t)h->R * 4);
+  m.ul = off; off += align_up((size_t)h->C * 4);
+  m.ut = off; off += align_up(HC * 4);
+  m.km = off; off += align_up(HR * 8 * 4);
+  m.nnz = off; off += 256;
+  m.bytes = off;
+  return m;
+}
+
+// Point the layer's array pointers into its scratch allocation (all null
+// when the layer has none on the device).
+void carve_meta(LayerState& L, const MetaLayout& m) {
+  if (!L.meta) {
+    L.mass = L.row_max = L.row_sum = nullptr;
+    L.kcount = L.keptcols = L.row_ptr = L.tile_of = L.union_cnt = L.union_list = L.utile = nullptr;
+    L.kmask = nullptr;
+    L.nnz_dev = nullptr;
+    return;
+  }
+  char* mb = static_cast<char*>(L.meta);
+  L.mass = (float*)(mb + m.mass);
+  L.row_max = (float*)(mb + m.max);
+  L.row_sum = (float*)(mb + m.sum);
+  L.kcount = (int*)(mb + m.kc);
+  L.keptcols = (int*)(mb + m.kept);
+  L.row_ptr = (int*)(mb + m.rp);
+  L.tile_of = (int*)(mb + m.tile);
+  L.union_cnt = (int*)(mb + m.uc);
+  L.union_list = (int*)(mb + m.ul);
+  L.utile = (int*)(mb + m.ut);
+  L.kmask = (uint32_t*)(mb + m.km);
+  L.nnz_dev = (long long*)(mb + m.nnz);
+}
+
 
 cudaEvent_t take_event(mf_bsr_t h) {
   if (!h->event_pool.empty()) {
@@ -357,38 +423,14 @@ int mf_compress(mf_bsr_t h, int layer, const void* q, const void* k, int dtype, 
     return fail(MF_ERR_UNSUPPORTED, "dtype %d with d = %d, B = %d is not built", dtype, d, B);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   LayerState& L = h->layers[layer];
-  if (L.meta || L.values || L.col_idx) release_layer(h, L, s);
+  if (L.meta || L.values || L.col_idx || L.offloaded || L.ready) release_layer(h, L, s);
 
-  const size_t HC = (size_t)h->H_s * h->C, HT = (size_t)h->H_s * h->T, HR = (size_t)h->H_s * h->R;
-  size_t off = 0;
-  const size_t o_mass = off; off += align_up(HC * 4);
-  const size_t o_max = off; off += align_up(HT * 4);
-  const size_t o_sum = off; off += align_up(HT * 4);
-  const size_t o_kc = off; off += align_up(HR * 4);
-  const size_t o_kept = off; off += align_up(HC * 4);
-  const size_t o_rp = off; off += align_up((HR + 1) * 4);
-  const size_t o_tile = off; off += align_up(HC * 4);
-  const size_t o_uc = off; off += align_up((size_t)h->R * 4);
-  const size_t o_ul = off; off += align_up((size_t)h->C * 4);
-  const size_t o_ut = off; off += align_up(HC * 4);
-  const size_t o_km = off; off += align_up(HR * 8 * 4);
-  const size_t o_nnz = off; off += 256;
-  L.meta = dev_alloc(h, off, s);
-  if (!L.meta) return fail(MF_ERR_OOM, "allocation of %zu bytes failed", off);
-  L.meta_bytes = off;
-  char* mb = static_cast<char*>(L.meta);
-  L.mass = (float*)(mb + o_mass);
-  L.row_max = (float*)(mb + o_max);
-  L.row_sum = (float*)(mb + o_sum);
-  L.kcount = (int*)(mb + o_kc);
-  L.keptcols = (int*)(mb + o_kept);
-  L.row_ptr = (int*)(mb + o_rp);
-  L.tile_of = (int*)(mb + o_tile);
-  L.union_cnt = (int*)(mb + o_uc);
-  L.union_list = (int*)(mb + o_ul);
-  L.utile = (int*)(mb + o_ut);
-  L.kmask = (uint32_t*)(mb + o_km);
-  L.nnz_dev = (long long*)(mb + o_nnz);
+  const size_t HC = (size_t)h->H_s * h->C;
+  const MetaLayout ml = meta_layout(h);
+  L.meta = dev_alloc(h, ml.bytes, s);
+  if (!L.meta) return fail(MF_ERR_OOM, "allocation of %zu bytes failed", ml.bytes);
+  L.meta_bytes = ml.bytes;
+  carve_meta(L, ml);
 
   CompressParams cp{};
   cp.rbs = h->rbs_d;
@@ -538,9 +580,15 @@ int mf_retrieve(mf_bsr_t h, const float* W, const void* v, void* o, int dtype, i
     if (sl < 0 || sl >= h->n_layers) return fail(MF_ERR_ARG, "layer_map[%d] = %d out of range", x, sl);
     const LayerState& L = h->layers[sl];
     if (!L.valid) return fail(MF_ERR_STATE, "sender layer %d has not been compressed", sl);
+    if (L.offloaded) return fail(MF_ERR_STATE, "sender layer %d is offloaded (mf_bsr_prefetch it)", sl);
     if (L.d != d) return fail(MF_ERR_ARG, "d = %d differs from the compressed layer's %d", d, L.d);
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // a prefetch may still be copying a layer in on another stream
+  for (int x = 0; x < n; ++x) {
+    const LayerState& L = h->layers[layer_map_host[x]];
+    if (L.ready) MF_CUDA(cudaStreamWaitEvent(s, L.ready, 0), "wait for the layer's prefetch");
+  }
   const size_t esz = (dtype == MF_DTYPE_BF16) ? 2 : 4;
   const size_t v_layer = (size_t)h->T * H_kv * d * esz;
   const size_t o_layer = (size_t)h->T * H_r * d * esz;
@@ -686,6 +734,7 @@ int mf_bsr_export(mf_bsr_t h, int layer, const int32_t** row_ptr, const int32_t*
   if (layer < 0 || layer >= h->n_layers) return fail(MF_ERR_ARG, "layer out of range");
   const LayerState& L = h->layers[layer];
   if (!L.valid) return fail(MF_ERR_STATE, "layer %d has not been compressed", layer);
+  if (L.offloaded) return fail(MF_ERR_STATE, "layer %d is offloaded", layer);
   if (row_ptr) *row_ptr = L.row_ptr;
   if (col_idx) *col_idx = L.col_idx;
   if (values) *values = L.values;
@@ -701,11 +750,13 @@ int mf_bsr_copy(mf_bsr_t h, int layer, int32_t* row_ptr, int32_t* col_idx, uint1
   if (layer < 0 || layer >= h->n_layers) return fail(MF_ERR_ARG, "layer out of range");
   LayerState& L = h->layers[layer];
   if (!L.valid) return fail(MF_ERR_STATE, "layer %d has not been compressed", layer);
+  if (L.offloaded) return fail(MF_ERR_STATE, "layer %d is offloaded", layer);
   if (col_idx || values) {
     const int rc = ensure_nnz(h, L);
     if (rc != MF_OK) return rc;
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (L.ready) MF_CUDA(cudaStreamWaitEvent(s, L.ready, 0), "wait for the layer's prefetch");
   const size_t HR = (size_t)h->H_s * h->R, HC = (size_t)h->H_s * h->C, HT = (size_t)h->H_s * h->T;
   auto cp = [&](void* dst, const void* src, size_t bytes) {
     return (dst && bytes) ? cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, s) : cudaSuccess;
@@ -723,6 +774,90 @@ int mf_bsr_release_layer(mf_bsr_t h, int layer) {
   if (!h) return fail(MF_ERR_ARG, "handle is NULL");
   if (layer < 0 || layer >= h->n_layers) return fail(MF_ERR_ARG, "layer out of range");
   release_layer(h, h->layers[layer], nullptr);
+  return MF_OK;
+}
+
+int mf_bsr_offload(mf_bsr_t h, int layer, void* stream) {
+  if (!h) return fail(MF_ERR_ARG, "handle is NULL");
+  if (layer < 0 || layer >= h->n_layers) return fail(MF_ERR_ARG, "layer out of range");
+  LayerState& L = h->layers[layer];
+  if (!L.valid) return fail(MF_ERR_STATE, "layer %d has not been compressed", layer);
+  if (L.offloaded) return MF_OK;
+  int rc = ensure_nnz(h, L);  // only the kept tiles travel
+  if (rc != MF_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (L.ready) MF_CUDA(cudaStreamWaitEvent(s, L.ready, 0), "wait for the layer's prefetch");
+  const size_t vbytes = (size_t)L.nnz * h->B * h->B * 2, cbytes = (size_t)L.nnz * 4;
+  if (!L.h_meta) MF_CUDA(cudaMallocHost(&L.h_meta, L.meta_bytes), "pinned host allocation");
+  if (L.h_values_cap < vbytes) {
+    if (L.h_values) cudaFreeHost(L.h_values);
+    L.h_values = nullptr;
+    L.h_values_cap = 0;
+    MF_CUDA(cudaMallocHost(&L.h_values, vbytes), "pinned host allocation");
+    L.h_values_cap = vbytes;
+  }
+  if (L.h_colidx_cap < cbytes) {
+    if (L.h_colidx) cudaFreeHost(L.h_colidx);
+    L.h_colidx = nullptr;
+    L.h_colidx_cap = 0;
+    MF_CUDA(cudaMallocHost(&L.h_colidx, cbytes), "pinned host allocation");
+    L.h_colidx_cap = cbytes;
+  }
+  MF_CUDA(cudaMemcpyAsync(L.h_meta, L.meta, L.meta_bytes, cudaMemcpyDeviceToHost, s), "offload copy");
+  if (vbytes) MF_CUDA(cudaMemcpyAsync(L.h_values, L.values, vbytes, cudaMemcpyDeviceToHost, s), "offload copy");
+  if (cbytes) MF_CUDA(cudaMemcpyAsync(L.h_colidx, L.col_idx, cbytes, cudaMemcpyDeviceToHost, s), "offload copy");
+  // the device buffers go back to the allocator behind the copies
+  dev_free(h, L.meta, s);
+  dev_free(h, L.values, s);
+  dev_free(h, L.col_idx, s);
+  L.meta = nullptr;
+  L.values = nullptr;
+  L.col_idx = nullptr;
+  carve_meta(L, meta_layout(h));  // null until the prefetch
+  if (!L.ready) MF_CUDA(cudaEventCreateWithFlags(&L.ready, cudaEventDisableTiming), "event");
+  MF_CUDA(cudaEventRecord(L.ready, s), "event record");
+  L.offloaded = true;
+  return MF_OK;
+}
+
+int mf_bsr_prefetch(mf_bsr_t h, int layer, void* stream) {
+  if (!h) return fail(MF_ERR_ARG, "handle is NULL");
+  if (layer < 0 || layer >= h->n_layers) return fail(MF_ERR_ARG, "layer out of range");
+  LayerState& L = h->layers[layer];
+  if (!L.valid) return fail(MF_ERR_STATE, "layer %d has not been compressed", layer);
+  if (!L.offloaded) return MF_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  MF_CUDA(cudaStreamWaitEvent(s, L.ready, 0), "wait for the layer's offload");
+  const int B = h->B;
+  const long long nnz = L.nnz;
+  const size_t vbytes = (size_t)nnz * B * B * 2, cbytes = (size_t)nnz * 4;
+  const MetaLayout ml = meta_layout(h);
+  L.meta = dev_alloc(h, ml.bytes, s);
+  L.values = (uint16_t*)dev_alloc(h, vbytes + (size_t)B * B * 2, s);
+  L.col_idx = (int*)dev_alloc(h, cbytes ? cbytes : 4, s);
+  if (!L.meta || !L.values || !L.col_idx) {
+    dev_free(h, L.meta, s);
+    dev_free(h, L.values, s);
+    dev_free(h, L.col_idx, s);
+    L.meta = nullptr;
+    L.values = nullptr;
+    L.col_idx = nullptr;
+    return fail(MF_ERR_OOM, "device allocation for the prefetch failed");
+  }
+  carve_meta(L, ml);
+  MF_CUDA(cudaMemcpyAsync(L.meta, L.h_meta, ml.bytes, cudaMemcpyHostToDevice, s), "prefetch copy");
+  if (vbytes) MF_CUDA(cudaMemcpyAsync(L.values, L.h_values, vbytes, cudaMemcpyHostToDevice, s), "prefetch copy");
+  if (cbytes) MF_CUDA(cudaMemcpyAsync(L.col_idx, L.h_colidx, cbytes, cudaMemcpyHostToDevice, s), "prefetch copy");
+  // the retrieval's all-zero tile, right after the kept ones
+  MF_CUDA(cudaMemsetAsync(reinterpret_cast<char*>(L.values) + vbytes, 0, (size_t)B * B * 2, s), "zero tile");
+  L.capacity = nnz;
+  L.values_bytes = vbytes;
+  L.colidx_bytes = cbytes;
+  const int rc = make_map(&L.pmap, L.values, B, (uint64_t)(nnz + 1) * B, (uint64_t)B * 2, 64, 64);
+  if (rc != MF_OK) return rc;
+  L.stream = s;
+  MF_CUDA(cudaEventRecord(L.ready, s), "event record");
+  L.offloaded = false;
   return MF_OK;
 }
 

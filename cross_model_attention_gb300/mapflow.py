@@ -21,7 +21,7 @@ MF_DTYPE_F32, MF_DTYPE_BF16 = 0, 1
 
 EXPORTED = ("mf_version", "mf_last_error", "mf_supported", "mf_bsr_create", "mf_bsr_destroy",
             "mf_compress", "mf_retrieve", "mf_bsr_info", "mf_bsr_export", "mf_bsr_copy",
-            "mf_bsr_release_layer", "mf_device_status", "mf_selftest_wait", "mf_profile",
+            "mf_bsr_release_layer", "mf_bsr_offload", "mf_bsr_prefetch", "mf_device_status", "mf_selftest_wait", "mf_profile",
             "mf_profile_read", "mf_profile_kinds", "mf_select_noalloc", "mf_bsr_set_exact")
 KERNELS = ("stats", "select", "scan", "pack", "union", "retrieve")
 
@@ -63,6 +63,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mf_bsr_export.argtypes = [vp, i32] + [ctypes.POINTER(vp)] * 6
     lib.mf_bsr_copy.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp, vp]
     lib.mf_bsr_release_layer.argtypes = [vp, i32]
+    lib.mf_bsr_offload.argtypes = [vp, i32, vp]
+    lib.mf_bsr_prefetch.argtypes = [vp, i32, vp]
     lib.mf_bsr_set_exact.argtypes = [vp, i32]
     lib.mf_device_status.argtypes = [vp, vp]
     lib.mf_selftest_wait.argtypes = [vp, i32, vp]
@@ -183,6 +185,14 @@ def mf_bsr_release_layer(h, layer: int) -> None:
     _check(load_library().mf_bsr_release_layer(h, layer))
 
 
+def mf_bsr_offload(h, layer: int, stream=None) -> None:
+    _check(load_library().mf_bsr_offload(h, layer, _stream(stream)))
+
+
+def mf_bsr_prefetch(h, layer: int, stream=None) -> None:
+    _check(load_library().mf_bsr_prefetch(h, layer, _stream(stream)))
+
+
 def mf_device_status(h, stream=None) -> None:
     _check(load_library().mf_device_status(h, _stream(stream)))
 
@@ -276,6 +286,14 @@ class BSR:
 
     def release_layer(self, layer: int) -> None:
         mf_bsr_release_layer(self.handle, layer)
+
+    def offload(self, layer: int, stream=None) -> None:
+        """Move the layer's BSR to pinned host memory (see mf_bsr_offload)."""
+        mf_bsr_offload(self.handle, layer, stream)
+
+    def prefetch(self, layer: int, stream=None) -> None:
+        """Bring an offloaded layer back to the device on `stream`."""
+        mf_bsr_prefetch(self.handle, layer, stream)
 
     def device_status(self, stream=None) -> None:
         mf_device_status(self.handle, stream)

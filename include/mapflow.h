@@ -225,6 +225,30 @@ MF_API int mf_bsr_copy(mf_bsr_t h, int layer, int32_t* row_ptr, int32_t* col_idx
 MF_API int mf_bsr_release_layer(mf_bsr_t h, int layer);
 
 /*
+ * mf_bsr_offload — move a compressed layer to pinned host memory owned by the
+ * handle and give its device buffers back to the allocator, asynchronously on
+ * `stream` (learns nnz first: one sync of the layer's stream if not known).
+ * Only the kept tiles travel.  The layer stays valid; mf_retrieve,
+ * mf_bsr_export and mf_bsr_copy reject it (MF_ERR_STATE) until
+ * mf_bsr_prefetch brings it back.  Work that reads the layer on other streams
+ * must be ordered before `stream` by the caller.
+ *
+ * mf_bsr_prefetch — bring an offloaded layer back to the device,
+ * asynchronously on `stream` (typically a copy stream, so that the transfer
+ * overlaps other work); mf_retrieve and mf_bsr_copy on any stream wait for its
+ * copies by themselves (an event recorded here).
+ *
+ * Together they let a caller keep on the device only the sender layers the
+ * next receiver layers read, and fetch the next ones while the receiver
+ * recomputes its first layers ([Article] "其二": the cached state is fetched
+ * while the receiver's first layers are recomputed).  No-ops on a layer that
+ * is already where asked.  Errors: MF_ERR_ARG, MF_ERR_STATE, MF_ERR_OOM,
+ * MF_ERR_CUDA.
+ */
+MF_API int mf_bsr_offload(mf_bsr_t h, int layer, void* stream);
+MF_API int mf_bsr_prefetch(mf_bsr_t h, int layer, void* stream);
+
+/*
  * mf_device_status — synchronise `stream` and read the handle's device
  * error word (set by bounded device-side waits).  Returns MF_OK,
  * MF_ERR_TIMEOUT (and clears the word), or MF_ERR_CUDA.

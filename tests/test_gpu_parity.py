@@ -279,6 +279,44 @@ def test_full_workload4_two_receivers():
     full_size(4)
 
 
+def test_offload_and_prefetch_roundtrip():
+    """A layer moved to host memory and brought back on another stream gives
+    the same BSR and the same retrieval output; while offloaded the
+    retrieval rejects it.  The prefetch shrinks the tile buffer to the kept
+    tiles (the zero tile moves to index nnz), which the retrieval must follow."""
+    seqlens = (700, 333)
+    T = sum(seqlens)
+    cu = np.concatenate([[0], np.cumsum(seqlens)]).astype(np.int32)
+    w = workloads.scaled(workloads.get(1), seqlens, sender_heads=8, sender_kv_heads=8)
+    x = synth.sender_qk(w, 1)
+    v = synth.random_v(T, 8, 128, 3)["v"][None]
+    W = synth.random_w(32, 8, 4)[None]
+    bsr = mapflow.BSR(2, T, 8, 64, cu)
+    gc.run_compress(bsr, 0, x, "bf16", 0.95)
+    gc.run_compress(bsr, 1, x, "bf16", 0.80)
+    before = gc.export_np(bsr, 0)
+    O_before = gc.run_retrieve(bsr, W, v, 32, "bf16", [0])
+    bsr.offload(0)
+    with pytest.raises(mapflow.MapFlowError) as ei:
+        gc.run_retrieve(bsr, W, v, 32, "bf16", [0])
+    assert ei.value.code == mapflow.MF_ERR_STATE
+    O_other = gc.run_retrieve(bsr, W, v, 32, "bf16", [1])  # the other layer is untouched
+    side = torch.cuda.Stream()
+    bsr.prefetch(0, stream=side)
+    O_after = gc.run_retrieve(bsr, W, v, 32, "bf16", [0])  # waits for the prefetch itself
+    after = gc.export_np(bsr, 0)
+    for key in ("row_ptr", "col_idx", "mass", "row_max", "row_sum"):
+        assert np.array_equal(before[key], after[key]), key
+    assert torch.equal(before["values_dev"], after["values_dev"])
+    assert np.array_equal(O_before, O_after)
+    assert not np.array_equal(O_other, O_after)
+    bsr.offload(0)
+    bsr.offload(0)  # a no-op when already offloaded
+    gc.run_compress(bsr, 0, x, "bf16", 0.95)  # recompressing an offloaded layer replaces it
+    assert np.array_equal(gc.run_retrieve(bsr, W, v, 32, "bf16", [0]), O_before)
+    bsr.close()
+
+
 def test_exact_and_bound_allocation_agree():
     """mf_compress sized exactly (one sync) and at the upper bound (no sync)
     produce the same BSR and the same retrieval output."""
