@@ -85,7 +85,7 @@ MF_API int mf_version(void);
 /* Message of the last failed call on this thread ("" if none). */
 MF_API const char* mf_last_error(void);
 
-/* Supported shapes of this build (for callers that want to check first). */
+/* Shapes the library supports (for callers that want to check first). */
 MF_API int mf_supported(int dtype, int d, int B);
 
 /*
