@@ -355,6 +355,45 @@ def dense_head_mapped(q64: np.ndarray, k64: np.ndarray, cu_seqlens: Sequence[int
 
 
 # --------------------------------------------------------------------------
+# Head-map calibration ([Summary] "MapFlow System Design" item 3: the head
+# map is a linear transformation of the sender's maps, fitted offline)
+# --------------------------------------------------------------------------
+
+
+def map_entries(q64: np.ndarray, k64: np.ndarray, grid: BlockGrid,
+                kept_of=None, causal: bool = True) -> np.ndarray:
+    """Every head's attention map over every packed sequence, flattened to
+    [H, sum_s L_s^2]; when kept_of(h, rb) is given, the blocks it does not
+    list are zero (the map as the BSR stores it)."""
+    T, H, d = q64.shape
+    Hk = k64.shape[1]
+    out = [[] for _ in range(H)]
+    cu = grid.cu
+    for s in range(len(cu) - 1):
+        a, b = int(cu[s]), int(cu[s + 1])
+        L = b - a
+        for h in range(H):
+            P = attention_rows(q64[a:b, h], k64[a:b, h // (H // Hk)], np.arange(L), causal)[0]
+            if kept_of is not None:
+                for bi in range(int(grid.nblocks[s])):
+                    r0, r1 = bi * grid.B, min(L, (bi + 1) * grid.B)
+                    P[r0:r1] *= kept_mask_rows(grid, kept_of(h, int(grid.rb_base[s]) + bi), bi, s, r1 - r0)
+            out[h].append(P.reshape(-1))
+    return np.stack([np.concatenate(x) for x in out])
+
+
+def calibrate_head_map(sender: np.ndarray, receiver: np.ndarray, ridge: float = 0.0) -> np.ndarray:
+    """W [H_r, H_s] minimising sum_i sum_m (receiver[i, m] - sum_h W[i, h]
+    sender[h, m])^2 + ridge * |W|^2 over the map entries m (reading: least
+    squares of the receiver's map against the sender heads' kept maps):
+    the normal equations (S S^T + ridge I) W^T = S R^T."""
+    S = np.asarray(sender, np.float64)
+    R = np.asarray(receiver, np.float64)
+    G = S @ S.T + ridge * np.eye(S.shape[0])
+    return np.linalg.solve(G, S @ R.T).T
+
+
+# --------------------------------------------------------------------------
 # Full-size helpers: sampled checks that stay exact per block-row
 # --------------------------------------------------------------------------
 

@@ -344,3 +344,53 @@ def test_tiles_are_probabilities():
                 assert np.abs(tile - ref).max() < 1e-14
                 # the tile's sum is the candidate's mass
                 assert abs(tile.sum() - bsr.mass[h, g.cand_ptr[rb] + bj]) < 1e-12
+
+
+# ------------------------------------------------------- head-map calibration
+
+def test_calibration_recovers_a_planted_map_exactly():
+    """Receiver maps that are exactly W_true times the sender maps give back
+    W_true (signed, non-square)."""
+    rng = np.random.default_rng(5)
+    S = rng.random((5, 400))
+    W_true = rng.standard_normal((3, 5))
+    W = orc.calibrate_head_map(S, W_true @ S)
+    assert np.allclose(W, W_true, atol=1e-10)
+
+
+def test_calibration_is_the_least_squares_solution():
+    """Against numpy's least-squares routine on the stacked system, with and
+    without the ridge (the ridge as sqrt(ridge) * I rows appended)."""
+    rng = np.random.default_rng(6)
+    S = rng.random((4, 300))
+    R = rng.random((6, 300))
+    W = orc.calibrate_head_map(S, R)
+    ref = np.linalg.lstsq(S.T, R.T, rcond=None)[0].T
+    assert np.allclose(W, ref, atol=1e-10)
+    lam = 0.37
+    Wr = orc.calibrate_head_map(S, R, ridge=lam)
+    A = np.concatenate([S.T, np.sqrt(lam) * np.eye(4)])
+    Bm = np.concatenate([R.T, np.zeros((4, 6))])
+    assert np.allclose(Wr, np.linalg.lstsq(A, Bm, rcond=None)[0].T, atol=1e-10)
+
+
+def test_map_entries_masks_dropped_blocks_and_rows_sum_to_one():
+    rng = np.random.default_rng(7)
+    cu = np.array([0, 100, 164])
+    q = rng.standard_normal((164, 2, 16))
+    k = rng.standard_normal((164, 2, 16))
+    g = orc.BlockGrid(cu, 32, True)
+    full = orc.map_entries(q, k, g)
+    # each sequence's L x L map has rows summing to one
+    assert np.allclose(full[:, :100 * 100].reshape(2, 100, 100).sum(-1), 1.0)
+    assert np.allclose(full[:, 100 * 100:].reshape(2, 64, 64).sum(-1), 1.0)
+    # dropping block column 0 of block-row 1 of sequence 0 (head 1) zeroes
+    # exactly rows 32..63, columns 0..31 of that head's map
+    kept = lambda h, rb: [bj for bj in range(int(g.ncand[rb])) if not (h == 1 and rb == 1 and bj == 0)]
+    part = orc.map_entries(q, k, g, kept)
+    m0 = part[1, :100 * 100].reshape(100, 100)
+    f0 = full[1, :100 * 100].reshape(100, 100)
+    assert np.all(m0[32:64, 0:32] == 0)
+    diff = (m0 != f0)
+    assert diff[32:64, 0:32].all() and diff.sum() == 32 * 32
+    assert np.array_equal(part[0], full[0])
