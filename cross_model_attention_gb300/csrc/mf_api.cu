@@ -861,6 +861,77 @@ int mf_bsr_prefetch(mf_bsr_t h, int layer, void* stream) {
   return MF_OK;
 }
 
+int mf_calibrate_head_map(mf_bsr_t sender, int sender_layer, mf_bsr_t receiver, int receiver_layer,
+                          float ridge, float* W_out, void* stream) {
+  if (!sender || !receiver || !W_out) return fail(MF_ERR_ARG, "NULL handle or W_out");
+  if (sender_layer < 0 || sender_layer >= sender->n_layers || receiver_layer < 0 ||
+      receiver_layer >= receiver->n_layers)
+    return fail(MF_ERR_ARG, "layer out of range");
+  if (!(ridge >= 0.f)) return fail(MF_ERR_ARG, "ridge must be >= 0");
+  if (sender->T != receiver->T || sender->B != receiver->B || sender->causal != receiver->causal ||
+      sender->cu != receiver->cu)
+    return fail(MF_ERR_ARG, "the two handles must share sequences, block size and causality");
+  const int H_s = sender->H_s, H_r = receiver->H_s;
+  if (H_s + H_r > kCalibRows)
+    return fail(MF_ERR_UNSUPPORTED, "H_s + H_r = %d > %d", H_s + H_r, kCalibRows);
+  LayerState& SL = sender->layers[sender_layer];
+  LayerState& RL = receiver->layers[receiver_layer];
+  if (!SL.valid || !RL.valid) return fail(MF_ERR_STATE, "both layers must be compressed");
+  if (SL.offloaded || RL.offloaded) return fail(MF_ERR_STATE, "both layers must be on the device");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (SL.ready) MF_CUDA(cudaStreamWaitEvent(s, SL.ready, 0), "wait for the layer's prefetch");
+  if (RL.ready) MF_CUDA(cudaStreamWaitEvent(s, RL.ready, 0), "wait for the layer's prefetch");
+  const int grid = calib_grid();
+  const size_t pbytes = (size_t)grid * kCalibRows * kCalibRows * sizeof(float);
+  float* partial = (float*)dev_alloc(sender, pbytes, s);
+  if (!partial) return fail(MF_ERR_OOM, "allocation of %zu bytes failed", pbytes);
+  CalibParams cp{SL.tile_of, SL.values, RL.tile_of, RL.values, sender->C, H_s, H_r, sender->B, partial};
+  std::vector<float> host((size_t)grid * kCalibRows * kCalibRows);
+  cudaError_t e = launch_calib_gram(cp, grid, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(host.data(), partial, pbytes, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  dev_free(sender, partial, s);
+  if (e != cudaSuccess) return cuda_fail(e, "calibration kernel");
+  // the CTAs' partial Gram matrices summed in a fixed order, in fp64
+  const int n = H_s + H_r;
+  std::vector<double> G((size_t)n * n, 0.0);
+  for (int b = 0; b < grid; ++b)
+    for (int i = 0; i < n; ++i)
+      for (int j = 0; j < n; ++j)
+        G[(size_t)i * n + j] += host[((size_t)b * kCalibRows + i) * kCalibRows + j];
+  // Cholesky factor of the sender block plus ridge: L L^T = G_ss + ridge I
+  std::vector<double> L((size_t)H_s * H_s, 0.0);
+  for (int i = 0; i < H_s; ++i) {
+    for (int j = 0; j <= i; ++j) {
+      double acc = G[(size_t)i * n + j] + (i == j ? (double)ridge : 0.0);
+      for (int k = 0; k < j; ++k) acc -= L[(size_t)i * H_s + k] * L[(size_t)j * H_s + k];
+      if (i == j) {
+        if (!(acc > 0.0))
+          return fail(MF_ERR_ARG, "the sender heads' Gram matrix is singular (pass ridge > 0)");
+        L[(size_t)i * H_s + i] = std::sqrt(acc);
+      } else {
+        L[(size_t)i * H_s + j] = acc / L[(size_t)j * H_s + j];
+      }
+    }
+  }
+  // each receiver head: solve L L^T w = C_i with C_i[h] = G[H_s + i][h]
+  std::vector<double> y(H_s), w(H_s);
+  for (int i = 0; i < H_r; ++i) {
+    for (int a = 0; a < H_s; ++a) {
+      double acc = G[(size_t)(H_s + i) * n + a];
+      for (int k = 0; k < a; ++k) acc -= L[(size_t)a * H_s + k] * y[k];
+      y[a] = acc / L[(size_t)a * H_s + a];
+    }
+    for (int a = H_s - 1; a >= 0; --a) {
+      double acc = y[a];
+      for (int k = a + 1; k < H_s; ++k) acc -= L[(size_t)k * H_s + a] * w[k];
+      w[a] = acc / L[(size_t)a * H_s + a];
+    }
+    for (int a = 0; a < H_s; ++a) W_out[(size_t)i * H_s + a] = (float)w[a];
+  }
+  return MF_OK;
+}
+
 int mf_device_status(mf_bsr_t h, void* stream) {
   if (!h) return fail(MF_ERR_ARG, "handle is NULL");
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -98,6 +98,20 @@ inline cudaError_t sm_count(int* out) {
 
 // -------------------------------------------------------------- launchers --
 // All return cudaError_t of the launch (cudaSuccess when enqueued).
+// Head-map calibration: Gram matrix of the stacked head maps of two BSR
+// layers over one block grid (rows 0..H_s-1 sender heads, then receiver heads).
+constexpr int kCalibRows = 96;
+struct CalibParams {
+  const int* s_tile_of;      // sender [C][H_s] kept tile index or -1
+  const uint16_t* s_values;  // sender tiles [.][B][B] bf16
+  const int* r_tile_of;      // receiver [C][H_r]
+  const uint16_t* r_values;
+  int C, H_s, H_r, B;
+  float* partial;            // [grid][kCalibRows][kCalibRows] per-CTA sums
+};
+int calib_grid();
+cudaError_t launch_calib_gram(const CalibParams& p, int grid, cudaStream_t s);
+
 // Statistics with two CTAs per SM (64-key S tiles) for rows of at most 128
 // candidate blocks; tk64 boxes are 64 keys high.
 bool stats2_supported(int max_cand);

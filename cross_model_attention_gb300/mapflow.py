@@ -21,7 +21,8 @@ MF_DTYPE_F32, MF_DTYPE_BF16 = 0, 1
 
 EXPORTED = ("mf_version", "mf_last_error", "mf_supported", "mf_bsr_create", "mf_bsr_destroy",
             "mf_compress", "mf_retrieve", "mf_bsr_info", "mf_bsr_export", "mf_bsr_copy",
-            "mf_bsr_release_layer", "mf_bsr_offload", "mf_bsr_prefetch", "mf_device_status", "mf_selftest_wait", "mf_profile",
+            "mf_bsr_release_layer", "mf_bsr_offload", "mf_bsr_prefetch", "mf_calibrate_head_map",
+            "mf_device_status", "mf_selftest_wait", "mf_profile",
             "mf_profile_read", "mf_profile_kinds", "mf_select_noalloc", "mf_bsr_set_exact")
 KERNELS = ("stats", "select", "scan", "pack", "union", "retrieve")
 
@@ -64,6 +65,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mf_bsr_copy.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp, vp]
     lib.mf_bsr_release_layer.argtypes = [vp, i32]
     lib.mf_bsr_offload.argtypes = [vp, i32, vp]
+    lib.mf_calibrate_head_map.argtypes = [vp, i32, vp, i32, ctypes.c_float, vp, vp]
     lib.mf_bsr_prefetch.argtypes = [vp, i32, vp]
     lib.mf_bsr_set_exact.argtypes = [vp, i32]
     lib.mf_device_status.argtypes = [vp, vp]
@@ -191,6 +193,17 @@ def mf_bsr_offload(h, layer: int, stream=None) -> None:
 
 def mf_bsr_prefetch(h, layer: int, stream=None) -> None:
     _check(load_library().mf_bsr_prefetch(h, layer, _stream(stream)))
+
+
+def calibrate_head_map(sender: "BSR", sender_layer: int, receiver: "BSR", receiver_layer: int,
+                       ridge: float = 0.0, stream=None) -> np.ndarray:
+    """Least-squares head map W [H_r, H_s] from two compressed layers over the
+    same sequences (see mf_calibrate_head_map)."""
+    W = np.zeros((receiver.H_s, sender.H_s), np.float32)
+    _check(load_library().mf_calibrate_head_map(
+        sender.handle, sender_layer, receiver.handle, receiver_layer, float(ridge),
+        W.ctypes.data_as(ctypes.c_void_p), _stream(stream)))
+    return W
 
 
 def mf_device_status(h, stream=None) -> None:

@@ -249,6 +249,27 @@ MF_API int mf_bsr_offload(mf_bsr_t h, int layer, void* stream);
 MF_API int mf_bsr_prefetch(mf_bsr_t h, int layer, void* stream);
 
 /*
+ * mf_calibrate_head_map — fit the head map W offline from two compressed
+ * layers over the same packed sequences ([Summary] "MapFlow System Design"
+ * item 3: the receiver's map of a reused layer is a linear transformation of
+ * the mapped sender layer's head maps, learned offline).  Reading: least
+ * squares over every map entry, each map as its BSR stores it (dropped blocks
+ * zero):  W = argmin sum_i |A_i - sum_h W[i,h] P_h|^2 + ridge |W|^2, where
+ * P_h are the `sender` layer's heads and A_i the `receiver` layer's (a handle
+ * made for the receiver's heads, typically compressed at p = 1).
+ *   W_out  HOST fp32 [H_r][H_s]
+ *   ridge  >= 0, added to the sender heads' Gram matrix
+ * The Gram matrices are accumulated on the GPU from the bf16 tiles (fp32
+ * partials, summed in fp64 on the host) and the H_s x H_s system is solved
+ * on the host (Cholesky, fp64).  Synchronises `stream`.  Both handles must
+ * share sequences, block size and causality; H_s + H_r <= 96.
+ * Errors: MF_ERR_ARG (incl. a singular Gram matrix: pass ridge > 0),
+ * MF_ERR_UNSUPPORTED, MF_ERR_STATE, MF_ERR_OOM, MF_ERR_CUDA.
+ */
+MF_API int mf_calibrate_head_map(mf_bsr_t sender, int sender_layer, mf_bsr_t receiver,
+                                 int receiver_layer, float ridge, float* W_out, void* stream);
+
+/*
  * mf_device_status — synchronise `stream` and read the handle's device
  * error word (set by bounded device-side waits).  Returns MF_OK,
  * MF_ERR_TIMEOUT (and clears the word), or MF_ERR_CUDA.

@@ -341,3 +341,99 @@ def test_exact_and_bound_allocation_agree():
         assert np.array_equal(a[key], b[key]), key
     assert torch.equal(a["values_dev"].view(torch.int16), b["values_dev"].view(torch.int16))
     assert np.array_equal(Oa, Ob)
+
+
+def _kept_of(ex, R):
+    rp, ci = ex["row_ptr"], ex["col_idx"]
+    return lambda h, rb: ci[rp[h * R + rb]:rp[h * R + rb + 1]]
+
+
+def _calib_bound(W_gpu, W_or, S, Rm, ridge):
+    """Both sides minimise J(W) = |R - W S|^2 + ridge |W|^2, the GPU on the
+    maps as stored (each entry within 2^-9 relative of the exact one after
+    the bf16 rounding; eps = 2^-8 leaves room for the fp32 softmax and Gram
+    sums).  sqrt(J) moves by at most eps (|R| + |W|_2 |S|) under that
+    perturbation, so the GPU's W can exceed the exact minimum by at most
+    eps (2 |R| + (|W_gpu|_2 + |W_or|_2) |S|)."""
+    eps = 2.0 ** -8
+
+    def sqrtJ(W):
+        return math.sqrt(np.sum((Rm - W @ S) ** 2) + ridge * np.sum(W ** 2))
+
+    slack = eps * (2 * np.linalg.norm(Rm) + (np.linalg.norm(W_gpu, 2) + np.linalg.norm(W_or, 2))
+                   * np.linalg.norm(S))
+    assert sqrtJ(W_or) <= sqrtJ(W_gpu) * (1 + 1e-9) + 1e-12, "the oracle is not the minimum"
+    assert sqrtJ(W_gpu) <= sqrtJ(W_or) + slack, (sqrtJ(W_gpu), sqrtJ(W_or), slack)
+    return sqrtJ(W_gpu), sqrtJ(W_or), slack
+
+
+@pytest.mark.parametrize("ridge", [0.0, 2.0])
+def test_calibrate_head_map_against_oracle(ridge):
+    """W fitted from a sender layer (p = 0.9) and another layer's maps
+    compressed with p = 1 against the oracle's fp64 least squares on the same
+    kept blocks."""
+    seqlens, B, Hs, Hr = (300, 129, 64), 64, 6, 5
+    T = sum(seqlens)
+    cu = np.concatenate([[0], np.cumsum(seqlens)]).astype(np.int32)
+    grid = orc.BlockGrid(cu, B, True)
+    ws = workloads.scaled(workloads.get(1), seqlens, sender_heads=Hs, sender_kv_heads=3)
+    wr = workloads.scaled(workloads.get(1), seqlens, sender_heads=Hr, sender_kv_heads=Hr, seed=7)
+    xs, xr = synth.sender_qk(ws, 1), synth.sender_qk(wr, 2)
+    sb, rbh = mapflow.BSR(1, T, Hs, B, cu), mapflow.BSR(1, T, Hr, B, cu)
+    gc.run_compress(sb, 0, xs, "bf16", 0.9)
+    gc.run_compress(rbh, 0, xr, "bf16", 1.0)
+    es, er = gc.export_np(sb, 0), gc.export_np(rbh, 0)
+    gc.check_structure(es, grid, Hs, 0.9)
+    gc.check_structure(er, grid, Hr, 1.0)
+    W_gpu = mapflow.calibrate_head_map(sb, 0, rbh, 0, ridge=ridge).astype(np.float64)
+    S = orc.map_entries(xs["q64"], xs["k64"], grid, _kept_of(es, grid.R))
+    Rm = orc.map_entries(xr["q64"], xr["k64"], grid, _kept_of(er, grid.R))
+    W_or = orc.calibrate_head_map(S, Rm, ridge)
+    assert W_gpu.shape == (Hr, Hs)
+    _calib_bound(W_gpu, W_or, S, Rm, ridge)
+    sb.close()
+    rbh.close()
+
+
+def test_calibrate_head_map_recovers_a_head_selection():
+    """Receiver heads that are copies of sender heads (same Q/K, same p, so
+    bitwise the same stored maps): W is the 0/1 selection matrix, which pins
+    the [H_r][H_s] layout and the head indexing.  The sender against itself
+    gives the identity."""
+    seqlens, B, Hs = (257, 64, 130), 64, 6
+    pick = [4, 0, 5, 2]
+    T = sum(seqlens)
+    cu = np.concatenate([[0], np.cumsum(seqlens)]).astype(np.int32)
+    ws = workloads.scaled(workloads.get(1), seqlens, sender_heads=Hs, sender_kv_heads=Hs)
+    xs = synth.sender_qk(ws, 3)
+    xr = {k: np.ascontiguousarray(v[:, pick]) for k, v in xs.items()}
+    sb, rbh = mapflow.BSR(1, T, Hs, B, cu), mapflow.BSR(1, T, len(pick), B, cu)
+    gc.run_compress(sb, 0, xs, "bf16", 0.9)
+    gc.run_compress(rbh, 0, xr, "bf16", 0.9)
+    sel = np.zeros((len(pick), Hs))
+    sel[np.arange(len(pick)), pick] = 1.0
+    W = mapflow.calibrate_head_map(sb, 0, rbh, 0)
+    assert np.abs(W - sel).max() < 1e-4, W
+    I = mapflow.calibrate_head_map(sb, 0, sb, 0)
+    assert np.abs(I - np.eye(Hs)).max() < 1e-4, I
+    sb.close()
+    rbh.close()
+
+
+def test_calibrate_head_map_rejects_bad_arguments():
+    cu = np.array([0, 200], np.int32)
+    a = mapflow.BSR(1, 200, 64, 64, cu)
+    b = mapflow.BSR(1, 200, 64, 64, cu)
+    c = mapflow.BSR(1, 200, 4, 64, np.array([0, 100, 200], np.int32))
+    d = mapflow.BSR(1, 200, 4, 64, cu)
+    with pytest.raises(mapflow.MapFlowError) as ei:
+        mapflow.calibrate_head_map(a, 0, b, 0)  # 128 rows
+    assert ei.value.code == mapflow.MF_ERR_UNSUPPORTED
+    with pytest.raises(mapflow.MapFlowError) as ei:
+        mapflow.calibrate_head_map(c, 0, d, 0)  # other sequences
+    assert ei.value.code == mapflow.MF_ERR_ARG
+    with pytest.raises(mapflow.MapFlowError) as ei:
+        mapflow.calibrate_head_map(d, 0, d, 0)  # not compressed
+    assert ei.value.code == mapflow.MF_ERR_STATE
+    for h in (a, b, c, d):
+        h.close()
