@@ -15,13 +15,14 @@
 #include <vector>
 
 #include "../../include/mapflow.h"
+#include "mf_handle.h"
 #include "mf_internal.cuh"
 
 using namespace mf;
 
-namespace {
+namespace mf {
 
-thread_local std::string g_last_error;
+static thread_local std::string g_last_error;
 
 int fail(int code, const char* fmt, ...) {
   char buf[512];
@@ -37,14 +38,8 @@ int cuda_fail(cudaError_t e, const char* what) {
   return fail(MF_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
-#define MF_CUDA(call, what)                     \
-  do {                                          \
-    cudaError_t e_ = (call);                    \
-    if (e_ != cudaSuccess) return cuda_fail(e_, what); \
-  } while (0)
-
 // ------------------------------------------------------------ tensor maps --
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
   std::call_once(once, [] {
@@ -61,8 +56,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // 2-D bf16 map: `inner` elements per row, `rows` rows, `stride` bytes between
 // rows; box = box_inner x box_rows; 128-byte swizzle; out-of-range reads give 0.
 int make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t stride,
-             uint32_t box_inner, uint32_t box_rows,
-             CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
+             uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swizzle) {
   auto fn = encode_fn();
   if (!fn) return fail(MF_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable (driver too old?)");
   cuuint64_t dims[2] = {inner, rows};
@@ -76,84 +70,9 @@ int make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, ui
   return MF_OK;
 }
 
-}  // namespace
+}  // namespace mf
 
-// --------------------------------------------------------------- handle --
-struct LayerState {
-  bool valid = false;
-  int dtype = -1;
-  int d = 0;
-  float p = 0.f;
-  long long nnz = 0;       // valid when nnz_known
-  bool nnz_known = false;
-  long long capacity = 0;  // tiles allocated for kept blocks (zero tile at this index)
-  cudaStream_t stream = nullptr;
-  void* meta = nullptr;    // one allocation carved into the arrays below
-  size_t meta_bytes = 0;
-  float* mass = nullptr;
-  float* row_max = nullptr;
-  float* row_sum = nullptr;
-  int* kcount = nullptr;
-  int* keptcols = nullptr;
-  int* row_ptr = nullptr;
-  int* tile_of = nullptr;
-  int* union_cnt = nullptr;
-  int* union_list = nullptr;
-  int* utile = nullptr;
-  uint32_t* kmask = nullptr;
-  long long* nnz_dev = nullptr;
-  int* col_idx = nullptr;
-  uint16_t* values = nullptr;
-  size_t values_bytes = 0, colidx_bytes = 0;
-  CUtensorMap pmap;  // values as [(nnz+1)*B rows][B cols], 64x64 boxes (per-group retrieval)
-  // while offloaded: the layer's arrays in pinned host memory owned by the
-  // handle (meta whole, the nnz kept tiles, col_idx); device pointers null
-  bool offloaded = false;
-  void* h_meta = nullptr;
-  void* h_values = nullptr;
-  void* h_colidx = nullptr;
-  size_t h_values_cap = 0, h_colidx_cap = 0;  // allocated host bytes
-  cudaEvent_t ready = nullptr;  // end of the last offload's or prefetch's copies
-};
-
-struct ProfRec {
-  int kind;
-  cudaEvent_t a, b;
-};
-
-struct mf_bsr_s {
-  bool exact_alloc = false;  // size the BSR exactly (one stream sync per layer)
-  unsigned prof_mask = 0;  // kernel kinds timed with events
-  long long launches[MF_K_COUNT] = {0};
-  std::vector<ProfRec> prof;
-  std::vector<cudaEvent_t> event_pool;
-  int n_layers = 0, T = 0, H_s = 0, B = 0, causal = 1, n_seqs = 0;
-  int R = 0, C = 0, max_cand = 0, n_tiles = 0, n_slabs = 0;
-  std::vector<int> cu;
-  std::vector<RowBlock> rbs;
-  std::vector<RowTile> tiles;
-  std::vector<RowSlab> slabs;
-  RowBlock* rbs_d = nullptr;
-  RowTile* tiles_d = nullptr;
-  RowSlab* slabs_d = nullptr;
-  int* err_d = nullptr;
-  long long* host_pinned = nullptr;  // [0] nnz, [1] error word
-  mf_alloc_fn alloc = nullptr;
-  mf_free_fn dealloc = nullptr;
-  void* ctx = nullptr;
-  std::vector<LayerState> layers;
-  // team retrieval's exchange ring (allocated on first use, sized for the
-  // device's team count)
-  void* ring = nullptr;
-  uint32_t* ring_flags = nullptr;
-  int ring_teams = 0;
-  // team retrieval's slab lists (longest-first onto the least-loaded team)
-  std::vector<int> team_slabs;
-  int* team_slabs_d = nullptr;
-  int team_slab_teams = 0, team_stride = 0;
-};
-
-namespace {
+namespace mf {
 
 void* dev_alloc(mf_bsr_t h, size_t bytes, cudaStream_t s) {
   if (bytes == 0) bytes = 256;
@@ -174,8 +93,9 @@ void dev_free(mf_bsr_t h, void* p, cudaStream_t s) {
 
 void release_layer(mf_bsr_t h, LayerState& L, cudaStream_t s) {
   dev_free(h, L.meta, s);
-  dev_free(h, L.values, s);
+  if (!L.view_bm) dev_free(h, L.values, s);  // a view's tiles belong to the block manager
   dev_free(h, L.col_idx, s);
+  if (L.view_bm) bm_unpin(L);
   if (L.ready) {
     cudaEventSynchronize(L.ready);  // no copy may still use the host buffers
     cudaEventDestroy(L.ready);
@@ -186,12 +106,7 @@ void release_layer(mf_bsr_t h, LayerState& L, cudaStream_t s) {
   L = LayerState();
 }
 
-size_t align_up(size_t x) { return (x + 255) & ~size_t(255); }
-
-// Byte offsets of a layer's arrays in its one scratch allocation ("meta").
-struct MetaLayout {
-  size_t mass, max, sum, kc, kept, rp, tile, uc, ul, ut, km, nnz, bytes;
-};
+static size_t align_up(size_t x) { return (x + 255) & ~size_t(255); }
 
 MetaLayout meta_layout(const mf_bsr_s* h) {
   const size_t HC = (size_t)h->H_s * h->C, HT = (size_t)h->H_s * h->T, HR = (size_t)h->H_s * h->R;
@@ -213,8 +128,6 @@ MetaLayout meta_layout(const mf_bsr_s* h) {
   return m;
 }
 
-// Point the layer's array pointers into its scratch allocation (all null
-// when the layer has none on the device).
 void carve_meta(LayerState& L, const MetaLayout& m) {
   if (!L.meta) {
     L.mass = L.row_max = L.row_sum = nullptr;
@@ -237,7 +150,9 @@ void carve_meta(LayerState& L, const MetaLayout& m) {
   L.kmask = (uint32_t*)(mb + m.km);
   L.nnz_dev = (long long*)(mb + m.nnz);
 }
+}  // namespace mf
 
+namespace {
 
 cudaEvent_t take_event(mf_bsr_t h) {
   if (!h->event_pool.empty()) {
@@ -734,6 +649,7 @@ int mf_bsr_export(mf_bsr_t h, int layer, const int32_t** row_ptr, const int32_t*
   if (layer < 0 || layer >= h->n_layers) return fail(MF_ERR_ARG, "layer out of range");
   const LayerState& L = h->layers[layer];
   if (!L.valid) return fail(MF_ERR_STATE, "layer %d has not been compressed", layer);
+  if (L.view_bm) return fail(MF_ERR_STATE, "layer %d is a block-manager view (its tiles are the manager's)", layer);
   if (L.offloaded) return fail(MF_ERR_STATE, "layer %d is offloaded", layer);
   if (row_ptr) *row_ptr = L.row_ptr;
   if (col_idx) *col_idx = L.col_idx;
@@ -750,6 +666,7 @@ int mf_bsr_copy(mf_bsr_t h, int layer, int32_t* row_ptr, int32_t* col_idx, uint1
   if (layer < 0 || layer >= h->n_layers) return fail(MF_ERR_ARG, "layer out of range");
   LayerState& L = h->layers[layer];
   if (!L.valid) return fail(MF_ERR_STATE, "layer %d has not been compressed", layer);
+  if (L.view_bm) return fail(MF_ERR_STATE, "layer %d is a block-manager view (its tiles are the manager's)", layer);
   if (L.offloaded) return fail(MF_ERR_STATE, "layer %d is offloaded", layer);
   if (col_idx || values) {
     const int rc = ensure_nnz(h, L);
@@ -782,6 +699,7 @@ int mf_bsr_offload(mf_bsr_t h, int layer, void* stream) {
   if (layer < 0 || layer >= h->n_layers) return fail(MF_ERR_ARG, "layer out of range");
   LayerState& L = h->layers[layer];
   if (!L.valid) return fail(MF_ERR_STATE, "layer %d has not been compressed", layer);
+  if (L.view_bm) return fail(MF_ERR_STATE, "layer %d is a block-manager view (its tiles are the manager's)", layer);
   if (L.offloaded) return MF_OK;
   int rc = ensure_nnz(h, L);  // only the kept tiles travel
   if (rc != MF_OK) return rc;

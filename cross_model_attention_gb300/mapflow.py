@@ -9,7 +9,7 @@ from __future__ import annotations
 
 import ctypes
 import os
-from typing import Dict, Optional, Sequence
+from typing import Dict, Optional, Sequence, Tuple
 
 import numpy as np
 
@@ -23,7 +23,9 @@ EXPORTED = ("mf_version", "mf_last_error", "mf_supported", "mf_bsr_create", "mf_
             "mf_compress", "mf_retrieve", "mf_bsr_info", "mf_bsr_export", "mf_bsr_copy",
             "mf_bsr_release_layer", "mf_bsr_offload", "mf_bsr_prefetch", "mf_calibrate_head_map",
             "mf_device_status", "mf_selftest_wait", "mf_profile",
-            "mf_profile_read", "mf_profile_kinds", "mf_select_noalloc", "mf_bsr_set_exact")
+            "mf_profile_read", "mf_profile_kinds", "mf_select_noalloc", "mf_bsr_set_exact",
+            "mf_prefix_hashes", "mf_bm_create", "mf_bm_destroy", "mf_bm_insert", "mf_bm_match",
+            "mf_bm_assemble", "mf_bm_stats")
 KERNELS = ("stats", "select", "scan", "pack", "union", "retrieve")
 
 
@@ -75,6 +77,16 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mf_profile.argtypes = [vp, i32]
     lib.mf_profile_kinds.argtypes = [vp, i32]
     lib.mf_profile_read.argtypes = [vp, i32, i64p, ctypes.POINTER(ctypes.c_double)]
+    u64p = ctypes.POINTER(ctypes.c_uint64)
+    lib.mf_prefix_hashes.argtypes = [ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32),
+                                     i32, i32, ctypes.c_uint64, u64p, ctypes.c_int64, i64p]
+    lib.mf_bm_create.argtypes = [ctypes.POINTER(vp), i32, i32, ctypes.c_int64, ALLOC_FN, FREE_FN,
+                                 vp, vp]
+    lib.mf_bm_destroy.argtypes = [vp]
+    lib.mf_bm_insert.argtypes = [vp, i32, vp, i32, u64p, i64p, vp]
+    lib.mf_bm_match.argtypes = [vp, i32, u64p, i32, ctypes.POINTER(i32)]
+    lib.mf_bm_assemble.argtypes = [vp, i32, u64p, vp, i32, vp]
+    lib.mf_bm_stats.argtypes = [vp, i64p]
     for name in EXPORTED:
         getattr(lib, name)
     _lib = lib
@@ -236,6 +248,86 @@ def mf_profile_read(h, kernel: int):
     n, ms = ctypes.c_int64(), ctypes.c_double()
     _check(load_library().mf_profile_read(h, kernel, ctypes.byref(n), ctypes.byref(ms)))
     return n.value, ms.value
+
+
+def mf_prefix_hashes(tokens, cu_seqlens: Sequence[int], B: int, seed: int = 0) -> np.ndarray:
+    """Chained prefix hashes of the B-token blocks of each packed sequence
+    (uint64 [R], the block-row order of a BSR handle with these cu_seqlens)."""
+    lib = load_library()
+    tok = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+    cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
+    if len(cu) < 2 or cu[-1] != len(tok):
+        raise ValueError("cu_seqlens must end at len(tokens)")
+    i32p = ctypes.POINTER(ctypes.c_int32)
+    n = ctypes.c_int64()
+    _check(lib.mf_prefix_hashes(tok.ctypes.data_as(i32p), cu.ctypes.data_as(i32p), len(cu) - 1, B,
+                                ctypes.c_uint64(seed), None, 0, ctypes.byref(n)))
+    out = np.zeros(n.value, np.uint64)
+    _check(lib.mf_prefix_hashes(tok.ctypes.data_as(i32p), cu.ctypes.data_as(i32p), len(cu) - 1, B,
+                                ctypes.c_uint64(seed), out.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64)),
+                                n.value, ctypes.byref(n)))
+    return out
+
+
+def _u64(hashes) -> Tuple[np.ndarray, "ctypes._Pointer"]:
+    a = np.ascontiguousarray(np.asarray(hashes, dtype=np.uint64))
+    return a, a.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64))
+
+
+class BlockManager:
+    """Owner of one mf_bm_t: block-rows of compressed layers cached under
+    prefix hashes in a device tile pool (see mf_bm_* in mapflow.h)."""
+
+    def __init__(self, H_s: int, B: int, tile_capacity: int, use_torch_allocator: bool = True,
+                 stream=None):
+        lib = load_library()
+        self.H_s, self.B, self.tile_capacity = H_s, B, int(tile_capacity)
+        h = ctypes.c_void_p()
+        if use_torch_allocator:
+            a, f = _torch_allocator()
+        else:
+            a, f = ALLOC_FN(), FREE_FN()
+        self._keep = (a, f)
+        _check(lib.mf_bm_create(ctypes.byref(h), H_s, B, self.tile_capacity, a, f, None,
+                                _stream(stream)))
+        self.handle = h
+
+    def insert(self, key_layer: int, bsr: "BSR", layer: int, hashes, stream=None) -> Tuple[int, int, int]:
+        """Caches the layer's block-rows; returns (inserted, already cached, evicted)."""
+        arr, ptr = _u64(hashes)
+        counts = (ctypes.c_int64 * 3)()
+        _check(load_library().mf_bm_insert(self.handle, key_layer, bsr.handle, layer, ptr, counts,
+                                           _stream(stream)))
+        return int(counts[0]), int(counts[1]), int(counts[2])
+
+    def match(self, key_layer: int, hashes) -> int:
+        arr, ptr = _u64(hashes)
+        n = ctypes.c_int()
+        _check(load_library().mf_bm_match(self.handle, key_layer, ptr, len(arr), ctypes.byref(n)))
+        return int(n.value)
+
+    def assemble(self, key_layer: int, hashes, bsr: "BSR", layer: int, stream=None) -> None:
+        """Makes `layer` of `bsr` a view of the cached block-rows `hashes`."""
+        arr, ptr = _u64(hashes)
+        _check(load_library().mf_bm_assemble(self.handle, key_layer, ptr, bsr.handle, layer,
+                                             _stream(stream)))
+
+    def stats(self) -> Dict[str, int]:
+        out = (ctypes.c_int64 * 7)()
+        _check(load_library().mf_bm_stats(self.handle, out))
+        keys = ("entries", "tiles_used", "tile_capacity", "hits", "misses", "evictions", "pinned")
+        return {k: int(v) for k, v in zip(keys, out)}
+
+    def close(self) -> None:
+        if self.handle is not None:
+            _check(load_library().mf_bm_destroy(self.handle))
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:  # noqa: BLE001
+            pass
 
 
 # ------------------------------------------------------ convenience class --

@@ -72,6 +72,7 @@ extern "C" {
 #define MF_DTYPE_BF16 1   /* bfloat16 (stored as uint16)                    */
 
 typedef struct mf_bsr_s* mf_bsr_t;   /* opaque; owns BSR state of n layers */
+typedef struct mf_bm_s* mf_bm_t;     /* opaque; block manager (prefix-hash cache) */
 
 /* Optional caller allocator (e.g. a framework's caching allocator).  Must
  * return a device pointer aligned to >= 256 bytes usable on `stream`, or
@@ -247,6 +248,90 @@ MF_API int mf_bsr_release_layer(mf_bsr_t h, int layer);
  */
 MF_API int mf_bsr_offload(mf_bsr_t h, int layer, void* stream);
 MF_API int mf_bsr_prefetch(mf_bsr_t h, int layer, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Block manager: compressed block-rows cached under prefix hashes
+ *
+ * [Summary] "Practical Implementation Details" (a block manager indexes the
+ * cache by prefix hash) and [Article] "其二" (states are indexed by hashes
+ * that carry the preceding context; a request finds the cached blocks of its
+ * shared prefix; one sender state serves several receivers).  Reading: under
+ * a causal mask block-row bi of a sequence (selection and kept tiles of every
+ * head) depends only on the tokens of blocks 0..bi, so it is keyed by the
+ * chained hash of those blocks and shared by every sequence that has the same
+ * prefix.  An entry is one block-row of one layer (the caller's layer key):
+ * its kept tiles of every head, stored once in a device tile pool, and their
+ * positions.  A view is an ordinary layer of a BSR handle whose tile table
+ * points into the pool; mf_retrieve reads it like a compressed layer, and
+ * mf_calibrate_head_map accepts it; export, copy and offload refuse it
+ * (MF_ERR_STATE).  Non-causal handles are refused (MF_ERR_UNSUPPORTED): their
+ * block-rows depend on the whole sequence.  A manager is not thread-safe.
+ * ------------------------------------------------------------------------- */
+
+/*
+ * mf_prefix_hashes — chained 64-bit hashes of the B-token blocks of each
+ * packed sequence: each block's hash mixes the previous block's hash (or
+ * `seed` for block 0), the block's length and its tokens (splitmix64
+ * finaliser), so a ragged last block never matches a full one.
+ *   tokens      HOST int32 [cu_seqlens[n_seqs]]
+ *   cu_seqlens  HOST int32 [n_seqs + 1]
+ *   hashes_out  HOST uint64 [capacity], filled in the block-row order of a
+ *               handle made with the same cu_seqlens and B; NULL: only *n_out
+ *   n_out       the number of block-rows R
+ * Errors: MF_ERR_ARG.
+ */
+MF_API int mf_prefix_hashes(const int32_t* tokens, const int32_t* cu_seqlens, int n_seqs, int B,
+                            uint64_t seed, uint64_t* hashes_out, int64_t capacity, int64_t* n_out);
+
+/*
+ * mf_bm_create / mf_bm_destroy — a manager for block-rows of H_s heads and
+ * block size B with a device pool of `tile_capacity` bf16 B x B tiles (plus
+ * one all-zero tile), allocated through alloc_fn (cudaMallocAsync if NULL)
+ * on `stream`.  Destroy fails with MF_ERR_STATE while a view pins entries.
+ * Errors: MF_ERR_ARG, MF_ERR_UNSUPPORTED (B), MF_ERR_OOM, MF_ERR_CUDA.
+ */
+MF_API int mf_bm_create(mf_bm_t* out, int H_s, int B, int64_t tile_capacity, mf_alloc_fn alloc_fn,
+                        mf_free_fn free_fn, void* alloc_ctx, void* stream);
+MF_API int mf_bm_destroy(mf_bm_t bm);
+
+/*
+ * mf_bm_insert — cache the block-rows of compressed `layer` of handle `h`
+ * under (key_layer, hashes[rb]), hashes HOST uint64 [R] as mf_prefix_hashes
+ * gives them.  Block-rows already cached are only marked used; new ones get
+ * pool slots (least recently used unpinned entries are evicted to make room)
+ * and their kept tiles are copied into the pool by a gather kernel on
+ * `stream`.  Reads the layer's tile table to the host (synchronises
+ * `stream`).  counts (optional, HOST int64 [3]): block-rows inserted, found
+ * cached, entries evicted.  A hash that names a cached block-row of another
+ * position or length is MF_ERR_ARG; more new tiles than the unpinned pool
+ * holds is MF_ERR_OOM (nothing is inserted).
+ */
+MF_API int mf_bm_insert(mf_bm_t bm, int key_layer, mf_bsr_t h, int layer, const uint64_t* hashes,
+                        int64_t* counts, void* stream);
+
+/*
+ * mf_bm_match — the length of the longest run hashes[0..k) cached under
+ * key_layer (the shared prefix, in block-rows), through *n_hit.
+ */
+MF_API int mf_bm_match(mf_bm_t bm, int key_layer, const uint64_t* hashes, int n, int* n_hit);
+
+/*
+ * mf_bm_assemble — make `layer` of handle `h` a view of the cached block-rows
+ * hashes[0..R) (HOST uint64 [R] in h's block-row order): the tile table and
+ * the retrieval's union tables are built on `stream` (one small kernel), the
+ * tiles stay in the pool.  The entries stay pinned (not evicted) until the
+ * layer is released, recompressed or re-assembled.  A hash that is not cached,
+ * or that names a block-row of another position or length, is MF_ERR_ARG.
+ */
+MF_API int mf_bm_assemble(mf_bm_t bm, int key_layer, const uint64_t* hashes, mf_bsr_t h, int layer,
+                          void* stream);
+
+/*
+ * mf_bm_stats — HOST int64 [7]: entries, pool tiles in use, pool capacity,
+ * block-rows found by mf_bm_match, mf_bm_match calls that stopped short,
+ * entries evicted, entries pinned by views.
+ */
+MF_API int mf_bm_stats(mf_bm_t bm, int64_t* out);
 
 /*
  * mf_calibrate_head_map — fit the head map W offline from two compressed
