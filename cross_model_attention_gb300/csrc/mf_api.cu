@@ -203,6 +203,13 @@ int mf_supported(int dtype, int d, int B) { return check_shapes(dtype, d, B); }
 int mf_bsr_create(mf_bsr_t* out, int n_layers, int T, int H_s, int B, int causal,
                   const int32_t* cu_seqlens_host, int n_seqs, mf_alloc_fn alloc_fn,
                   mf_free_fn free_fn, void* alloc_ctx) {
+  return mf_bsr_create_chunked(out, n_layers, T, H_s, B, causal, cu_seqlens_host, nullptr, n_seqs,
+                               alloc_fn, free_fn, alloc_ctx);
+}
+
+int mf_bsr_create_chunked(mf_bsr_t* out, int n_layers, int T, int H_s, int B, int causal,
+                          const int32_t* cu_seqlens_host, const int32_t* q_begin_host, int n_seqs,
+                          mf_alloc_fn alloc_fn, mf_free_fn free_fn, void* alloc_ctx) {
   if (!out) return fail(MF_ERR_ARG, "out is NULL");
   *out = nullptr;
   if (n_layers < 1 || T < 1 || H_s < 1 || n_seqs < 1 || !cu_seqlens_host)
@@ -221,6 +228,17 @@ int mf_bsr_create(mf_bsr_t* out, int n_layers, int T, int H_s, int B, int causal
   }
   if (cu_seqlens_host[n_seqs] != T)
     return fail(MF_ERR_ARG, "cu_seqlens[n_seqs] = %d != T = %d", cu_seqlens_host[n_seqs], T);
+  if (q_begin_host) {
+    if (!causal) return fail(MF_ERR_UNSUPPORTED, "query chunks need a causal mask");
+    long long rows = 0;
+    for (int s = 0; s < n_seqs; ++s) {
+      const int L = cu_seqlens_host[s + 1] - cu_seqlens_host[s], qb = q_begin_host[s];
+      if (qb < 0 || qb > L || (qb % 128 != 0 && qb != L))
+        return fail(MF_ERR_ARG, "q_begin[%d] = %d must be a multiple of 128 in [0, %d], or %d", s, qb, L, L);
+      rows += L - qb;
+    }
+    if (rows == 0) return fail(MF_ERR_ARG, "the chunks hold no query rows");
+  }
 
   mf_bsr_t h = new mf_bsr_s();
   h->n_layers = n_layers;
@@ -233,20 +251,26 @@ int mf_bsr_create(mf_bsr_t* out, int n_layers, int T, int H_s, int B, int causal
   h->dealloc = free_fn;
   h->ctx = alloc_ctx;
   h->cu.assign(cu_seqlens_host, cu_seqlens_host + n_seqs + 1);
+  h->q_begin.assign(n_seqs, 0);
+  if (q_begin_host) h->q_begin.assign(q_begin_host, q_begin_host + n_seqs);
   long long cand = 0;
   for (int s = 0; s < n_seqs; ++s) {
     const int start = h->cu[s], L = h->cu[s + 1] - h->cu[s];
+    if (h->q_begin[s] == L) continue;  // an empty chunk
     const int nb = (L + B - 1) / B;
-    const int rb_first = (int)h->rbs.size();
-    for (int bi = 0; bi < nb; ++bi) {
+    // query block-rows from q_begin on (a chunk over a prefix); keys from 0
+    const int b0 = h->q_begin[s] / B;
+    const int rb_first = (int)h->rbs.size();  // the handle's index of block-row b0
+    for (int bi = b0; bi < nb; ++bi) {
       h->rbs.push_back(RowBlock{start, L, bi, (int)cand});
       cand += causal ? bi + 1 : nb;
       h->max_cand = std::max(h->max_cand, causal ? bi + 1 : nb);
       for (int half = 0; half < B / 64; ++half)
-        if (bi * B + half * 64 < L) h->slabs.push_back(RowSlab{rb_first + bi, half});
+        if (bi * B + half * 64 < L) h->slabs.push_back(RowSlab{rb_first + bi - b0, half});
     }
     const int nt = (L + 127) / 128;
-    for (int tl = 0; tl < nt; ++tl) h->tiles.push_back(RowTile{start, L, tl, rb_first + tl * (128 / B)});
+    for (int tl = h->q_begin[s] / 128; tl < nt; ++tl)
+      h->tiles.push_back(RowTile{start, L, tl, rb_first + tl * (128 / B) - b0});
   }
   if (cand > (1ll << 30)) {
     delete h;
@@ -787,7 +811,7 @@ int mf_calibrate_head_map(mf_bsr_t sender, int sender_layer, mf_bsr_t receiver, 
     return fail(MF_ERR_ARG, "layer out of range");
   if (!(ridge >= 0.f)) return fail(MF_ERR_ARG, "ridge must be >= 0");
   if (sender->T != receiver->T || sender->B != receiver->B || sender->causal != receiver->causal ||
-      sender->cu != receiver->cu)
+      sender->cu != receiver->cu || sender->q_begin != receiver->q_begin)
     return fail(MF_ERR_ARG, "the two handles must share sequences, block size and causality");
   const int H_s = sender->H_s, H_r = receiver->H_s;
   if (H_s + H_r > kCalibRows)

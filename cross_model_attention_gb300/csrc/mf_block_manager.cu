@@ -150,8 +150,8 @@ void bm_unpin(LayerState& L) {
 
 extern "C" {
 
-int mf_prefix_hashes(const int32_t* tokens, const int32_t* cu_seqlens, int n_seqs, int B, uint64_t seed,
-                     uint64_t* hashes_out, int64_t capacity, int64_t* n_out) {
+int mf_prefix_hashes(const int32_t* tokens, const int32_t* cu_seqlens, const int32_t* q_begin, int n_seqs, int B,
+                     uint64_t seed, uint64_t* hashes_out, int64_t capacity, int64_t* n_out) {
   if (!tokens || !cu_seqlens || !n_out) return fail(MF_ERR_ARG, "NULL pointer argument");
   if (n_seqs < 1 || B < 1) return fail(MF_ERR_ARG, "n_seqs and B must be >= 1");
   if (cu_seqlens[0] != 0) return fail(MF_ERR_ARG, "cu_seqlens[0] must be 0");
@@ -159,7 +159,10 @@ int mf_prefix_hashes(const int32_t* tokens, const int32_t* cu_seqlens, int n_seq
   for (int s = 0; s < n_seqs; ++s) {
     const int L = cu_seqlens[s + 1] - cu_seqlens[s];
     if (L < 0) return fail(MF_ERR_ARG, "cu_seqlens must be non-decreasing");
-    R += (L + B - 1) / B;
+    const int qb = q_begin ? q_begin[s] : 0;
+    if (qb < 0 || qb > L || (qb % B != 0 && qb != L))
+      return fail(MF_ERR_ARG, "q_begin[%d] = %d is neither a block start nor the sequence's end", s, qb);
+    if (qb < L) R += (L + B - 1) / B - qb / B;
   }
   *n_out = R;
   if (!hashes_out) return MF_OK;  // size query
@@ -168,11 +171,12 @@ int mf_prefix_hashes(const int32_t* tokens, const int32_t* cu_seqlens, int n_seq
   for (int s = 0; s < n_seqs; ++s) {
     const int a = cu_seqlens[s], L = cu_seqlens[s + 1] - a;
     uint64_t h = mix64(seed ^ 0x6A09E667F3BCC909ull);
+    const int qb = q_begin ? q_begin[s] : 0;
     for (int b0 = 0; b0 < L; b0 += B) {
       const int n = std::min(B, L - b0);
       h = mix64(h ^ (0x9E3779B97F4A7C15ull * (uint64_t)n));  // the block's length
       for (int i = 0; i < n; ++i) h = mix64(h ^ (uint64_t)(uint32_t)tokens[a + b0 + i]);
-      hashes_out[r++] = h;
+      if (b0 >= qb) hashes_out[r++] = h;  // the chain runs over the prefix too
     }
   }
   return MF_OK;

@@ -71,6 +71,7 @@ struct mf_bsr_s {
   int n_layers = 0, T = 0, H_s = 0, B = 0, causal = 1, n_seqs = 0;
   int R = 0, C = 0, max_cand = 0, n_tiles = 0, n_slabs = 0;
   std::vector<int> cu;
+  std::vector<int> q_begin;  // per sequence: first query row (0, or a chunk's start)
   std::vector<mf::RowBlock> rbs;
   std::vector<mf::RowTile> tiles;
   std::vector<mf::RowSlab> slabs;

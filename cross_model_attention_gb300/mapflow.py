@@ -24,8 +24,8 @@ EXPORTED = ("mf_version", "mf_last_error", "mf_supported", "mf_bsr_create", "mf_
             "mf_bsr_release_layer", "mf_bsr_offload", "mf_bsr_prefetch", "mf_calibrate_head_map",
             "mf_device_status", "mf_selftest_wait", "mf_profile",
             "mf_profile_read", "mf_profile_kinds", "mf_select_noalloc", "mf_bsr_set_exact",
-            "mf_prefix_hashes", "mf_bm_create", "mf_bm_destroy", "mf_bm_insert", "mf_bm_match",
-            "mf_bm_assemble", "mf_bm_stats")
+            "mf_bsr_create_chunked", "mf_prefix_hashes", "mf_bm_create", "mf_bm_destroy",
+            "mf_bm_insert", "mf_bm_match", "mf_bm_assemble", "mf_bm_stats")
 KERNELS = ("stats", "select", "scan", "pack", "union", "retrieve")
 
 
@@ -79,7 +79,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mf_profile_read.argtypes = [vp, i32, i64p, ctypes.POINTER(ctypes.c_double)]
     u64p = ctypes.POINTER(ctypes.c_uint64)
     lib.mf_prefix_hashes.argtypes = [ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32),
-                                     i32, i32, ctypes.c_uint64, u64p, ctypes.c_int64, i64p]
+                                     vp, i32, i32, ctypes.c_uint64, u64p, ctypes.c_int64, i64p]
+    lib.mf_bsr_create_chunked.argtypes = [ctypes.POINTER(vp), i32, i32, i32, i32, i32,
+                                          ctypes.POINTER(ctypes.c_int32), vp, i32, ALLOC_FN,
+                                          FREE_FN, vp]
     lib.mf_bm_create.argtypes = [ctypes.POINTER(vp), i32, i32, ctypes.c_int64, ALLOC_FN, FREE_FN,
                                  vp, vp]
     lib.mf_bm_destroy.argtypes = [vp]
@@ -145,8 +148,10 @@ def mf_supported(dtype: int, d: int, B: int) -> bool:
 
 
 def mf_bsr_create(n_layers: int, T: int, H_s: int, B: int, causal: bool,
-                  cu_seqlens: Sequence[int], use_torch_allocator: bool = True):
-    """Returns (handle, keepalive); keepalive holds the allocator callbacks."""
+                  cu_seqlens: Sequence[int], use_torch_allocator: bool = True,
+                  q_begin: Optional[Sequence[int]] = None):
+    """Returns (handle, keepalive); keepalive holds the allocator callbacks.
+    With q_begin the handle covers query chunks (mf_bsr_create_chunked)."""
     lib = load_library()
     cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
     h = ctypes.c_void_p()
@@ -154,9 +159,15 @@ def mf_bsr_create(n_layers: int, T: int, H_s: int, B: int, causal: bool,
         a, f = _torch_allocator()
     else:
         a, f = ALLOC_FN(), FREE_FN()
-    rc = lib.mf_bsr_create(ctypes.byref(h), n_layers, T, H_s, B, int(causal),
-                           cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), len(cu) - 1,
-                           a, f, None)
+    i32p = ctypes.POINTER(ctypes.c_int32)
+    if q_begin is None:
+        rc = lib.mf_bsr_create(ctypes.byref(h), n_layers, T, H_s, B, int(causal),
+                               cu.ctypes.data_as(i32p), len(cu) - 1, a, f, None)
+    else:
+        qb = np.ascontiguousarray(np.asarray(q_begin, dtype=np.int32))
+        rc = lib.mf_bsr_create_chunked(ctypes.byref(h), n_layers, T, H_s, B, int(causal),
+                                       cu.ctypes.data_as(i32p), qb.ctypes.data_as(ctypes.c_void_p),
+                                       len(cu) - 1, a, f, None)
     _check(rc)
     return h, (a, f)
 
@@ -250,22 +261,27 @@ def mf_profile_read(h, kernel: int):
     return n.value, ms.value
 
 
-def mf_prefix_hashes(tokens, cu_seqlens: Sequence[int], B: int, seed: int = 0) -> np.ndarray:
+def mf_prefix_hashes(tokens, cu_seqlens: Sequence[int], B: int, seed: int = 0,
+                     q_begin: Optional[Sequence[int]] = None) -> np.ndarray:
     """Chained prefix hashes of the B-token blocks of each packed sequence
-    (uint64 [R], the block-row order of a BSR handle with these cu_seqlens)."""
+    (uint64 [R], the block-row order of a BSR handle with these cu_seqlens and
+    q_begin)."""
     lib = load_library()
     tok = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
     cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
     if len(cu) < 2 or cu[-1] != len(tok):
         raise ValueError("cu_seqlens must end at len(tokens)")
+    qb = None if q_begin is None else np.ascontiguousarray(np.asarray(q_begin, dtype=np.int32))
+    qb_ptr = None if qb is None else qb.ctypes.data_as(ctypes.c_void_p)
     i32p = ctypes.POINTER(ctypes.c_int32)
     n = ctypes.c_int64()
-    _check(lib.mf_prefix_hashes(tok.ctypes.data_as(i32p), cu.ctypes.data_as(i32p), len(cu) - 1, B,
-                                ctypes.c_uint64(seed), None, 0, ctypes.byref(n)))
+    _check(lib.mf_prefix_hashes(tok.ctypes.data_as(i32p), cu.ctypes.data_as(i32p), qb_ptr, len(cu) - 1,
+                                B, ctypes.c_uint64(seed), None, 0, ctypes.byref(n)))
     out = np.zeros(n.value, np.uint64)
-    _check(lib.mf_prefix_hashes(tok.ctypes.data_as(i32p), cu.ctypes.data_as(i32p), len(cu) - 1, B,
-                                ctypes.c_uint64(seed), out.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64)),
-                                n.value, ctypes.byref(n)))
+    _check(lib.mf_prefix_hashes(tok.ctypes.data_as(i32p), cu.ctypes.data_as(i32p), qb_ptr, len(cu) - 1,
+                                B, ctypes.c_uint64(seed),
+                                out.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64)), n.value,
+                                ctypes.byref(n)))
     return out
 
 
@@ -335,11 +351,13 @@ class BSR:
     """Owner of one mf_bsr_t (compressed sender state of several layers)."""
 
     def __init__(self, n_layers: int, T: int, H_s: int, B: int, cu_seqlens: Sequence[int],
-                 causal: bool = True, use_torch_allocator: bool = True):
+                 causal: bool = True, use_torch_allocator: bool = True,
+                 q_begin: Optional[Sequence[int]] = None):
         self.n_layers, self.T, self.H_s, self.B, self.causal = n_layers, T, H_s, B, causal
         self.cu_seqlens = [int(x) for x in cu_seqlens]
+        self.q_begin = None if q_begin is None else [int(x) for x in q_begin]
         self.handle, self._keep = mf_bsr_create(n_layers, T, H_s, B, causal, self.cu_seqlens,
-                                                use_torch_allocator)
+                                                use_torch_allocator, self.q_begin)
         self.d: Optional[int] = None
 
     def compress(self, layer: int, q, k, p: float, stream=None) -> None:

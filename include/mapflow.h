@@ -112,6 +112,29 @@ MF_API int mf_bsr_create(mf_bsr_t* out, int n_layers, int T, int H_s, int B, int
                   const int32_t* cu_seqlens_host, int n_seqs,
                   mf_alloc_fn alloc_fn, mf_free_fn free_fn, void* alloc_ctx);
 
+/*
+ * mf_bsr_create_chunked — a handle whose query rows start at q_begin[s] in
+ * each sequence while its keys start at 0: a prefill chunk over a prefix
+ * ([Article], the paragraph after "其三": the system runs inside a serving
+ * engine with chunked prefill; reading: a chunk's block-rows are the full
+ * sequence's block-rows from q_begin on, computed against every earlier key).  mf_compress then
+ * computes, and mf_retrieve writes, only the chunk's rows: q and o keep the
+ * full packed layout [T, ...] (rows before q_begin are neither read nor
+ * written), k and v cover the whole prefix.  Block-row order, R and C count
+ * only the chunk's block-rows.  With a block manager this is how a request
+ * whose prefix is cached compresses only its new block-rows
+ * (mf_prefix_hashes with the same q_begin names them).
+ *   q_begin_host  HOST int32 [n_seqs], each a multiple of 128 in [0, L_s],
+ *                 or L_s (an empty chunk); NULL: mf_bsr_create.  The chunks
+ *                 must hold >= 1 row
+ * Causal only (MF_ERR_UNSUPPORTED otherwise).  Other arguments and errors as
+ * mf_bsr_create.
+ */
+MF_API int mf_bsr_create_chunked(mf_bsr_t* out, int n_layers, int T, int H_s, int B, int causal,
+                                 const int32_t* cu_seqlens_host, const int32_t* q_begin_host,
+                                 int n_seqs, mf_alloc_fn alloc_fn, mf_free_fn free_fn,
+                                 void* alloc_ctx);
+
 /* Release every buffer of the handle (waits for the device first). */
 MF_API void mf_bsr_destroy(mf_bsr_t h);
 
@@ -275,13 +298,19 @@ MF_API int mf_bsr_prefetch(mf_bsr_t h, int layer, void* stream);
  * finaliser), so a ragged last block never matches a full one.
  *   tokens      HOST int32 [cu_seqlens[n_seqs]]
  *   cu_seqlens  HOST int32 [n_seqs + 1]
+ *   q_begin     HOST int32 [n_seqs] or NULL: hashes only of the block-rows
+ *               from q_begin[s] on (a multiple of B, or L_s), as a chunked handle
+ *               (mf_bsr_create_chunked) orders them; the chain still runs
+ *               over the tokens before
  *   hashes_out  HOST uint64 [capacity], filled in the block-row order of a
- *               handle made with the same cu_seqlens and B; NULL: only *n_out
+ *               handle made with the same cu_seqlens, q_begin and B; NULL:
+ *               only *n_out
  *   n_out       the number of block-rows R
  * Errors: MF_ERR_ARG.
  */
-MF_API int mf_prefix_hashes(const int32_t* tokens, const int32_t* cu_seqlens, int n_seqs, int B,
-                            uint64_t seed, uint64_t* hashes_out, int64_t capacity, int64_t* n_out);
+MF_API int mf_prefix_hashes(const int32_t* tokens, const int32_t* cu_seqlens, const int32_t* q_begin,
+                            int n_seqs, int B, uint64_t seed, uint64_t* hashes_out, int64_t capacity,
+                            int64_t* n_out);
 
 /*
  * mf_bm_create / mf_bm_destroy — a manager for block-rows of H_s heads and

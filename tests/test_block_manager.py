@@ -1,10 +1,13 @@
-"""Block manager: prefix hashes (host, no GPU) and block-row states cached
-under them, assembled into BSR views that the retrieval reads (GPU).
+"""Block manager and chunked prefill: prefix hashes (host, no GPU), block-row
+states cached under them and assembled into BSR views that the retrieval
+reads, and handles whose query rows are a chunk over a prefix (GPU).
 
 Reading tested here: under a causal mask block-row bi of a sequence depends
 only on the tokens of blocks 0..bi, so two requests that share a prefix share
-the compressed states of its full blocks, and a view assembled from cached
-block-rows retrieves exactly what the request's own compressed BSR does."""
+the compressed states of its full blocks, a view assembled from cached
+block-rows retrieves exactly what the request's own compressed BSR does, and
+a chunk's block-rows are exactly the full sequence's block-rows from the
+chunk's start on."""
 import numpy as np
 import pytest
 
@@ -61,6 +64,27 @@ def test_prefix_hashes_ragged_block_is_not_a_full_block(lib):
     # empty sequences have no block-rows; the size query answers alone
     h = mapflow.mf_prefix_hashes(a, [0, 0, len(a), len(a)], B)
     assert np.array_equal(h, ha)
+
+
+def test_prefix_hashes_of_a_chunk_continue_the_chain(lib):
+    a, b = _tokens(700, 6), _tokens(333, 7)
+    cu = [0, 700, 1033]
+    full = mapflow.mf_prefix_hashes(np.concatenate([a, b]), cu, B)
+    chunk = mapflow.mf_prefix_hashes(np.concatenate([a, b]), cu, B, q_begin=[384, 128])
+    nb_a = (700 + B - 1) // B
+    assert np.array_equal(chunk, np.concatenate([full[384 // B:nb_a], full[nb_a + 128 // B:]]))
+    with pytest.raises(mapflow.MapFlowError):
+        mapflow.mf_prefix_hashes(a, [0, 700], B, q_begin=[100])  # not a block start
+    # a chunk that starts at a ragged end is empty
+    assert len(mapflow.mf_prefix_hashes(np.concatenate([a, b]), cu, B, q_begin=[700, 0])) == 6
+
+
+def test_chunked_handle_rejects_bad_chunks(lib):
+    cu = [0, 700, 1033]
+    for qb, causal in (([100, 0], True), ([768, 0], True), ([700, 333], True), ([128, 0], False)):
+        with pytest.raises(mapflow.MapFlowError) as ei:
+            mapflow.BSR(1, 1033, 8, B, cu, causal=causal, q_begin=qb)
+        assert ei.value.code in (mapflow.MF_ERR_ARG, mapflow.MF_ERR_UNSUPPORTED)
 
 
 # ------------------------------------------------------------------ GPU --
@@ -190,3 +214,97 @@ def test_eviction_spares_pinned_and_current_entries(lib):
     bm.close()
     A.close()
     Bh.close()
+
+
+@pytest.mark.gpu
+def test_chunk_rows_equal_the_full_sequence_rows(lib):
+    """A chunked handle (query rows from q_begin, keys from 0) compresses and
+    retrieves exactly the full handle's block-rows from q_begin on, and writes
+    no output row before it; one sequence's chunk is empty."""
+    gc.dev()
+    seqlens, qb, Hs = (700, 333, 200), (384, 128, 200), 8
+    T = sum(seqlens)
+    cu = np.concatenate([[0], np.cumsum(seqlens)]).astype(np.int32)
+    w = workloads.scaled(workloads.get(1), seqlens, sender_heads=Hs, sender_kv_heads=4)
+    x = synth.sender_qk(w, 1)
+    F = mapflow.BSR(1, T, Hs, B, cu)
+    Cn = mapflow.BSR(1, T, Hs, B, cu, q_begin=qb)
+    gc.run_compress(F, 0, x, "bf16", 0.9)
+    gc.run_compress(Cn, 0, x, "bf16", 0.9)
+    grid = orc.BlockGrid(cu, B, True)
+    exF, exC = gc.export_np(F, 0), gc.export_np(Cn, 0)
+    gc.check_structure(exF, grid, Hs, 0.9)
+    rows_f = [int(grid.rb_base[s]) + bi for s in range(3) if qb[s] < seqlens[s]
+              for bi in range(qb[s] // B, (seqlens[s] + B - 1) // B)]
+    RC = len(rows_f)
+    assert Cn.info(0)[1] == Hs * RC
+    cand_c = np.concatenate([[0], np.cumsum([grid.cand_ptr[r + 1] - grid.cand_ptr[r] for r in rows_f])])
+    massF = exF["mass"].reshape(Hs, grid.C)
+    massC = exC["mass"].reshape(Hs, int(cand_c[-1]))
+    for h in range(Hs):
+        for j, rf in enumerate(rows_f):
+            rc_, rf_ = h * RC + j, h * grid.R + rf
+            a0, a1 = exC["row_ptr"][rc_], exC["row_ptr"][rc_ + 1]
+            b0, b1 = exF["row_ptr"][rf_], exF["row_ptr"][rf_ + 1]
+            assert np.array_equal(exC["col_idx"][a0:a1], exF["col_idx"][b0:b1])
+            assert np.array_equal(gc.tiles(exC, range(a0, a1)), gc.tiles(exF, range(b0, b1)))
+            assert np.array_equal(massC[h, cand_c[j]:cand_c[j + 1]],
+                                  massF[h, grid.cand_ptr[rf]:grid.cand_ptr[rf + 1]])
+    chunk_rows = np.concatenate([np.arange(cu[s] + qb[s], cu[s + 1]) for s in range(3)])
+    other = np.setdiff1d(np.arange(T), chunk_rows)
+    for key in ("row_max", "row_sum"):
+        assert np.array_equal(exC[key][:, chunk_rows], exF[key][:, chunk_rows])
+    for Hr, Hkv in ((32, 8), (8, 2)):
+        v = synth.random_v(T, Hkv, 128, 50 + Hkv)["v"][None]
+        W = synth.random_w(Hr, Hs, 60 + Hr)[None]
+        OF = gc.run_retrieve(F, W, v, Hr, "bf16", [0])[0]
+        OC = gc.run_retrieve(Cn, W, v, Hr, "bf16", [0])[0]
+        assert np.array_equal(OC[chunk_rows], OF[chunk_rows])
+        assert np.isnan(OC[other]).all()
+    F.close()
+    Cn.close()
+
+
+@pytest.mark.gpu
+def test_cached_prefix_then_chunk(lib):
+    """The serving flow: request 1 is compressed and cached; request 2 finds
+    its 6-block prefix cached, compresses only the chunk after it, caches
+    that, and a view of all its block-rows retrieves exactly what a full
+    compression of request 2 does; a receiver chunk over the cached prefix
+    gets exactly those rows."""
+    gc.dev()
+    Hs, LP = 8, 6 * B
+    xa, ta = _request(LP, 116, 41)
+    xb, tb = _request(LP, 316, 42, xa, ta)
+    Ta, Tb = len(ta), len(tb)
+    ha = mapflow.mf_prefix_hashes(ta, [0, Ta], B)
+    hb = mapflow.mf_prefix_hashes(tb, [0, Tb], B)
+    A = mapflow.BSR(1, Ta, Hs, B, [0, Ta])
+    gc.run_compress(A, 0, xa, "bf16", 0.9)
+    bm = mapflow.BlockManager(Hs, B, 4096)
+    bm.insert(0, A, 0, ha)
+    k = bm.match(0, hb)
+    assert k == LP // B
+    q0 = (k * B) // 128 * 128
+    Cn = mapflow.BSR(1, Tb, Hs, B, [0, Tb], q_begin=[q0])
+    gc.run_compress(Cn, 0, xb, "bf16", 0.9)
+    hc = mapflow.mf_prefix_hashes(tb, [0, Tb], B, q_begin=[q0])
+    assert np.array_equal(hc, hb[q0 // B:])
+    assert bm.insert(0, Cn, 0, hc) == (len(hc), 0, 0)
+    V = mapflow.BSR(1, Tb, Hs, B, [0, Tb])
+    bm.assemble(0, hb, V, 0)
+    F = mapflow.BSR(1, Tb, Hs, B, [0, Tb])
+    gc.run_compress(F, 0, xb, "bf16", 0.9)
+    own, view = _retrieve_both(F, Tb, Hs, 7), _retrieve_both(V, Tb, Hs, 7)
+    for o, v in zip(own, view):
+        assert np.array_equal(o, v)
+    VC = mapflow.BSR(1, Tb, Hs, B, [0, Tb], q_begin=[q0])
+    bm.assemble(0, hc, VC, 0)
+    for o, c in zip(own, _retrieve_both(VC, Tb, Hs, 7)):
+        assert np.array_equal(c[:, q0:], o[:, q0:]) and np.isnan(c[:, :q0]).all()
+    for h in (V, VC):
+        h.close()
+    bm.close()
+    for h in (A, Cn, F):
+        h.close()
+
