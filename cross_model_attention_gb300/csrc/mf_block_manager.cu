@@ -187,6 +187,8 @@ int mf_bm_create(mf_bm_t* out, int H_s, int B, int64_t tile_capacity, mf_alloc_f
   if (!out) return fail(MF_ERR_ARG, "out is NULL");
   *out = nullptr;
   if (H_s < 1) return fail(MF_ERR_ARG, "H_s must be >= 1");
+  if ((alloc_fn == nullptr) != (free_fn == nullptr))
+    return fail(MF_ERR_ARG, "alloc_fn and free_fn must both be set or both be NULL");
   if (B != 64 && B != 128) return fail(MF_ERR_UNSUPPORTED, "block size %d (supported: 64, 128)", B);
   if (tile_capacity < 1 || tile_capacity >= (1ll << 31) - 1) return fail(MF_ERR_ARG, "tile_capacity out of range");
   auto bm = std::make_unique<mf_bm_s>();

@@ -81,6 +81,29 @@ def test_null_handle_and_pointers(lib):
     lib.mf_bsr_destroy(None)
 
 
+def test_later_entry_points_validate_on_the_host(lib):
+    E = mapflow
+    vp = ctypes.c_void_p
+    h = vp()
+    A, F = mapflow.ALLOC_FN(), mapflow.FREE_FN()
+    assert lib.mf_bm_create(None, 8, 64, 16, A, F, None, None) == E.MF_ERR_ARG
+    assert lib.mf_bm_create(ctypes.byref(h), 0, 64, 16, A, F, None, None) == E.MF_ERR_ARG
+    assert lib.mf_bm_create(ctypes.byref(h), 8, 32, 16, A, F, None, None) == E.MF_ERR_UNSUPPORTED
+    assert lib.mf_bm_create(ctypes.byref(h), 8, 64, 0, A, F, None, None) == E.MF_ERR_ARG
+    assert lib.mf_bm_create(ctypes.byref(h), 8, 64, 16,
+                            mapflow.ALLOC_FN(lambda n, c, s: None), F, None, None) == E.MF_ERR_ARG
+    assert lib.mf_bm_insert(None, 0, None, 0, None, None, None) == E.MF_ERR_ARG
+    n = ctypes.c_int()
+    assert lib.mf_bm_match(None, 0, None, 0, ctypes.byref(n)) == E.MF_ERR_ARG
+    assert lib.mf_bm_assemble(None, 0, None, None, 0, None) == E.MF_ERR_ARG
+    assert lib.mf_bm_stats(None, None) == E.MF_ERR_ARG
+    assert lib.mf_bm_destroy(None) == E.MF_OK
+    assert lib.mf_calibrate_head_map(None, 0, None, 0, ctypes.c_float(0.0), None, None) == E.MF_ERR_ARG
+    assert lib.mf_bsr_offload(None, 0, None) == E.MF_ERR_ARG
+    assert lib.mf_bsr_prefetch(None, 0, None) == E.MF_ERR_ARG
+    assert lib.mf_last_error().decode()
+
+
 def test_allocator_pair_must_match(lib):
     cu = np.array([0, 64], np.int32)
     h = ctypes.c_void_p()
