@@ -132,3 +132,45 @@ def test_mass_pin_catches_block_offset(monkeypatch):
     monkeypatch.setattr(orc, "block_masses", off_by_one)
     with pytest.raises(AssertionError):
         pins.test_uniform_causal_closed_form(64, 8)
+
+
+# ------------------------------------------------------- head-map calibration
+def _calibrate_factory(mode):
+    def calibrate_head_map(sender, receiver, ridge=0.0):
+        S = np.asarray(sender, np.float64)
+        R = np.asarray(receiver, np.float64)
+        G = S @ S.T
+        if mode == "ridge_dropped":
+            pass
+        elif mode == "ridge_everywhere":
+            G = G + ridge  # added to every entry instead of the diagonal
+        else:
+            G = G + ridge * np.eye(S.shape[0])
+        if mode == "receiver_gram":
+            return np.linalg.solve(G, S @ R.T).T @ (R @ R.T) / max(np.trace(R @ R.T), 1.0)
+        return np.linalg.solve(G, S @ R.T).T
+    return calibrate_head_map
+
+
+@pytest.mark.parametrize("mode,pin", [
+    ("ridge_dropped", pins.test_calibration_is_the_least_squares_solution),
+    ("ridge_everywhere", pins.test_calibration_is_the_least_squares_solution),
+    ("receiver_gram", pins.test_calibration_recovers_a_planted_map_exactly),
+])
+def test_calibration_pins_catch_mistakes(monkeypatch, mode, pin):
+    monkeypatch.setattr(orc, "calibrate_head_map", _calibrate_factory(mode))
+    with pytest.raises((AssertionError, ValueError)):
+        pin()
+
+
+def test_map_entries_pin_catches_an_off_by_one_block_mask(monkeypatch):
+    def shifted_mask(grid, kept, bi, s, n_rows):
+        # plausible mistake: kept block bj marks the columns of block bj + 1
+        L = int(grid.lens[s])
+        mk = np.zeros((n_rows, L))
+        for bj in kept:
+            mk[:, min(L, (bj + 1) * grid.B):min(L, (bj + 2) * grid.B)] = 1.0
+        return mk
+    monkeypatch.setattr(orc, "kept_mask_rows", shifted_mask)
+    with pytest.raises(AssertionError):
+        pins.test_map_entries_masks_dropped_blocks_and_rows_sum_to_one()
