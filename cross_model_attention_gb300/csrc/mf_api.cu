@@ -823,24 +823,28 @@ int mf_calibrate_head_map(mf_bsr_t sender, int sender_layer, mf_bsr_t receiver, 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (SL.ready) MF_CUDA(cudaStreamWaitEvent(s, SL.ready, 0), "wait for the layer's prefetch");
   if (RL.ready) MF_CUDA(cudaStreamWaitEvent(s, RL.ready, 0), "wait for the layer's prefetch");
-  const int grid = calib_grid();
-  const size_t pbytes = (size_t)grid * kCalibRows * kCalibRows * sizeof(float);
-  float* partial = (float*)dev_alloc(sender, pbytes, s);
-  if (!partial) return fail(MF_ERR_OOM, "allocation of %zu bytes failed", pbytes);
-  CalibParams cp{SL.tile_of, SL.values, RL.tile_of, RL.values, sender->C, H_s, H_r, sender->B, partial};
-  std::vector<float> host((size_t)grid * kCalibRows * kCalibRows);
-  cudaError_t e = launch_calib_gram(cp, grid, s);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(host.data(), partial, pbytes, cudaMemcpyDeviceToHost, s);
-  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-  dev_free(sender, partial, s);
-  if (e != cudaSuccess) return cuda_fail(e, "calibration kernel");
-  // the CTAs' partial Gram matrices summed in a fixed order, in fp64
   const int n = H_s + H_r;
-  std::vector<double> G((size_t)n * n, 0.0);
-  for (int b = 0; b < grid; ++b)
-    for (int i = 0; i < n; ++i)
-      for (int j = 0; j < n; ++j)
-        G[(size_t)i * n + j] += host[((size_t)b * kCalibRows + i) * kCalibRows + j];
+  const int grid = calib_grid(sender->C);
+  const size_t gbytes = (size_t)n * n * sizeof(double);
+  const size_t pbytes = (size_t)grid * kCalibRows * kCalibRows * sizeof(float);
+  char* scratch = (char*)dev_alloc(sender, gbytes + pbytes, s);
+  if (!scratch) return fail(MF_ERR_OOM, "allocation of %zu bytes failed", gbytes + pbytes);
+  double* G_d = reinterpret_cast<double*>(scratch);
+  CalibParams cp{SL.tile_of, SL.values, RL.tile_of, RL.values, sender->C, H_s, H_r, sender->B,
+                 reinterpret_cast<float*>(scratch + gbytes), sender->err_d};
+  // the Gram matrix of [sender heads; receiver heads] over every stored entry
+  std::vector<double> G((size_t)n * n);
+  cudaError_t e = launch_calib_gram(cp, grid, G_d, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(G.data(), G_d, gbytes, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(&sender->host_pinned[1], sender->err_d, sizeof(int), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  dev_free(sender, scratch, s);
+  if (e != cudaSuccess) return cuda_fail(e, "calibration kernel");
+  if (static_cast<int>(sender->host_pinned[1] & 0xffffffff)) {
+    cudaMemsetAsync(sender->err_d, 0, sizeof(int), s);
+    return fail(MF_ERR_TIMEOUT, "a device-side wait timed out in the calibration kernel");
+  }
   // Cholesky factor of the sender block plus ridge: L L^T = G_ss + ridge I
   std::vector<double> L((size_t)H_s * H_s, 0.0);
   for (int i = 0; i < H_s; ++i) {

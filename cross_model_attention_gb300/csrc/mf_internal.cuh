@@ -108,9 +108,13 @@ struct CalibParams {
   const uint16_t* r_values;
   int C, H_s, H_r, B;
   float* partial;            // [grid][kCalibRows][kCalibRows] per-CTA sums
+  int* err;                  // device error word (bounded waits)
 };
-int calib_grid();
-cudaError_t launch_calib_gram(const CalibParams& p, int grid, cudaStream_t s);
+// CTAs for C candidate blocks (two per SM at most, none idle).
+int calib_grid(int C);
+// The Gram kernel, then the fixed-order fp64 sum of its partials into
+// G [n][n], n = H_s + H_r.
+cudaError_t launch_calib_gram(const CalibParams& p, int grid, double* G, cudaStream_t s);
 
 // Statistics with two CTAs per SM (64-key S tiles) for rows of at most 128
 // candidate blocks; tk64 boxes are 64 keys high.
