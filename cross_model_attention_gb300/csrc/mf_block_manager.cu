@@ -283,11 +283,24 @@ int mf_bm_insert(mf_bm_t bm, int key_layer, mf_bsr_t h, int layer, const uint64_
     fresh.push_back(std::move(nr));
   }
   if (need > (size_t)bm->cap) return fail(MF_ERR_OOM, "%zu new tiles exceed the pool's %lld", need, bm->cap);
-  if (!make_room(bm, need, call_tick, &evicted))
+  int sms = 0;
+  MF_CUDA(sm_count(&sms), "device query");
+  // the device copy list first: nothing below changes the cache until every
+  // step that can fail has succeeded (all or nothing)
+  int2* pairs_d = nullptr;
+  if (need > 0) {
+    pairs_d = (int2*)pool_alloc(bm, need * sizeof(int2), s);
+    if (!pairs_d) return fail(MF_ERR_OOM, "copy list allocation failed");
+  }
+  if (!make_room(bm, need, call_tick, &evicted)) {
+    pool_free(bm, pairs_d, s);
     return fail(MF_ERR_OOM, "the pool has %zu free tiles for %zu new ones; the rest are pinned or in use by this call",
                 bm->free_slots.size(), need);
+  }
   std::vector<int2> pairs;
   pairs.reserve(need);
+  std::vector<std::unique_ptr<BmEntry>> made;
+  made.reserve(fresh.size());
   for (NewRow& nr : fresh) {
     const RowBlock& rbk = h->rbs[nr.rb];
     auto e = std::make_unique<BmEntry>();
@@ -298,32 +311,35 @@ int mf_bm_insert(mf_bm_t bm, int key_layer, mf_bsr_t h, int layer, const uint64_
     e->where = std::move(nr.where);
     e->slots.resize(e->where.size());
     for (size_t i = 0; i < e->slots.size(); ++i) {
-      e->slots[i] = bm->free_slots.back();
-      bm->free_slots.pop_back();
+      e->slots[i] = bm->free_slots[bm->free_slots.size() - 1 - pairs.size()];
       pairs.push_back(make_int2(nr.src[i], e->slots[i]));
     }
+    made.push_back(std::move(e));
+  }
+  if (!pairs.empty()) {
+    cudaError_t e = cudaMemcpyAsync(pairs_d, pairs.data(), pairs.size() * sizeof(int2), cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) {
+      const int grid = (int)std::min<size_t>(pairs.size(), (size_t)sms * 8);
+      const int tile_u4 = bm->B * bm->B * 2 / 16;
+      bm_gather_tiles_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(L.values),
+                                                  reinterpret_cast<uint4*>(bm->pool), pairs_d, (int)pairs.size(),
+                                                  tile_u4);
+      e = cudaGetLastError();
+    }
+    // the host list was pageable: the copy has consumed it on return
+    pool_free(bm, pairs_d, s);
+    if (e != cudaSuccess) return cuda_fail(e, "tile gather");
+  }
+  // commit: the slots leave the free list and the entries enter the index
+  bm->free_slots.resize(bm->free_slots.size() - pairs.size());
+  for (auto& e : made) {
     e->tick = ++bm->tick;
     bm->lru.insert({e->tick, e.get()});
-    bm->index.emplace(mf_bm_s::Key{key_layer, e->hash}, std::move(e));
+    const uint64_t hsh = e->hash;
+    bm->index.emplace(mf_bm_s::Key{key_layer, hsh}, std::move(e));
     ++inserted;
   }
   bm->d = L.d;
-  if (!pairs.empty()) {
-    int2* pairs_d = (int2*)pool_alloc(bm, pairs.size() * sizeof(int2), s);
-    if (!pairs_d) return fail(MF_ERR_OOM, "copy list allocation failed");
-    MF_CUDA(cudaMemcpyAsync(pairs_d, pairs.data(), pairs.size() * sizeof(int2), cudaMemcpyHostToDevice, s),
-            "copy list");
-    int sms = 0;
-    MF_CUDA(sm_count(&sms), "device query");
-    const int grid = (int)std::min<size_t>(pairs.size(), (size_t)sms * 8);
-    const int tile_u4 = bm->B * bm->B * 2 / 16;
-    bm_gather_tiles_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint4*>(L.values),
-                                                reinterpret_cast<uint4*>(bm->pool), pairs_d, (int)pairs.size(),
-                                                tile_u4);
-    MF_CUDA(cudaGetLastError(), "tile gather kernel");
-    // the host list above was pageable: the copy has consumed it on return
-    pool_free(bm, pairs_d, s);
-  }
   if (counts) {
     counts[0] = inserted;
     counts[1] = present;
