@@ -394,3 +394,39 @@ def test_map_entries_masks_dropped_blocks_and_rows_sum_to_one():
     diff = (m0 != f0)
     assert diff[32:64, 0:32].all() and diff.sum() == 32 * 32
     assert np.array_equal(part[0], full[0])
+
+
+# ------------------------------------------- prefix sharing (block manager)
+
+def test_prefix_block_rows_do_not_depend_on_the_continuation():
+    """Reading behind the prefix-hash cache: with a causal mask, block-row bi
+    (masses, kept set, tiles, row statistics) depends only on the tokens of
+    blocks 0..bi, so two sequences that share three full blocks share the
+    states of those block-rows; without the mask they do not."""
+    rng = np.random.default_rng(21)
+    B, d, H, P = 16, 16, 2, 48
+    qa, ka = rng.standard_normal((P + 20, H, d)), rng.standard_normal((P + 20, H, d))
+    qb, kb = rng.standard_normal((P + 37, H, d)), rng.standard_normal((P + 37, H, d))
+    qb[:P], kb[:P] = qa[:P], ka[:P]
+    for causal in (True, False):
+        A = orc.compress(qa, ka, [0, P + 20], B, 0.9, causal)
+        Bq = orc.compress(qb, kb, [0, P + 37], B, 0.9, causal)
+        same = True
+        for h in range(H):
+            for rb in range(P // B):
+                ka_, kb_ = A.kept(h, rb), Bq.kept(h, rb)
+                ca, cb = A.grid.cand_ptr[rb], Bq.grid.cand_ptr[rb]
+                na = A.grid.cand_ptr[rb + 1] - ca
+                nb_ = Bq.grid.cand_ptr[rb + 1] - cb
+                ma, mb = A.mass[h, ca:ca + na], Bq.mass[h, cb:cb + nb_]
+                if na != nb_ or not np.allclose(ma, mb, rtol=1e-13, atol=0):
+                    same = False
+                    continue
+                assert ka_ == kb_
+                ta = A.tiles[A.row_ptr[h * A.grid.R + rb]:A.row_ptr[h * A.grid.R + rb + 1]]
+                tb = Bq.tiles[Bq.row_ptr[h * Bq.grid.R + rb]:Bq.row_ptr[h * Bq.grid.R + rb + 1]]
+                assert np.allclose(ta, tb, rtol=1e-13, atol=1e-300)
+            for key in ("m", "l"):
+                if not np.allclose(getattr(A, key)[h, :P], getattr(Bq, key)[h, :P], rtol=1e-13):
+                    same = False
+        assert same == causal
