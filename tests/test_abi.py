@@ -125,3 +125,17 @@ def test_library_has_no_driver_link(lib):
     out = subprocess.run(["readelf", "-d", mapflow.LIB_PATH], capture_output=True, text=True).stdout
     needed = [l for l in out.splitlines() if "NEEDED" in l]
     assert needed and not any("libcuda" in l for l in needed)
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """No fallback: without the built library every entry point raises."""
+    monkeypatch.setattr(mapflow, "_lib", None)
+    missing = str(tmp_path / "libmapflow.so")
+    with pytest.raises(ImportError):
+        mapflow.load_library(missing)
+    monkeypatch.setattr(mapflow, "LIB_PATH", missing)
+    monkeypatch.setattr(mapflow.load_library, "__defaults__", (missing,))
+    with pytest.raises(ImportError):
+        mapflow.mf_version()
+    with pytest.raises(ImportError):
+        mapflow.mf_prefix_hashes(np.zeros(4, np.int32), [0, 4], 64)
