@@ -117,7 +117,8 @@ MF_API int mf_bsr_create(mf_bsr_t* out, int n_layers, int T, int H_s, int B, int
  * each sequence while its keys start at 0: a prefill chunk over a prefix
  * ([Article], the paragraph after "其三": the system runs inside a serving
  * engine with chunked prefill; reading: a chunk's block-rows are the full
- * sequence's block-rows from q_begin on, computed against every earlier key).  mf_compress then
+ * sequence's block-rows from q_begin on, computed against every earlier
+ * key).  mf_compress then
  * computes, and mf_retrieve writes, only the chunk's rows: q and o keep the
  * full packed layout [T, ...] (rows before q_begin are neither read nor
  * written), k and v cover the whole prefix.  Block-row order, R and C count
