@@ -4,9 +4,8 @@
 // Why it exists: mf_compress allocates its buffers (through the caller's
 // allocator or cudaMallocAsync).  Some callers cannot allocate at the moment
 // they need a selection: serving engines that reserve nearly all device
-// memory for their KV cache at start-up and forbid further cudaMalloc, code
-// running inside CUDA stream capture (where cudaMalloc/cudaFree are illegal),
-// and latency-critical loops that cannot afford the implicit device
+// memory for their KV cache at start-up and forbid further cudaMalloc, and
+// latency-critical loops that cannot afford the implicit device
 // synchronisation of cudaFree.  This entry point takes the block masses and
 // the output arrays from the caller and keeps its own intermediates (the
 // per-row kept counts and kept-column lists, and the block-row table) in one

@@ -239,8 +239,26 @@ def mf_selftest_wait(h, limit_ms: int, stream=None) -> None:
 
 def mf_select_noalloc(mass, cu_seqlens: Sequence[int], H_s: int, B: int, causal: bool,
                       p: float, row_ptr, col_idx, nnz, stream=None) -> None:
-    """Selection into caller buffers with no device allocation (see mapflow.h)."""
+    """Selection into caller buffers with no device allocation (see mapflow.h).
+
+    The library sees only pointers, so the buffer sizes, dtypes and devices
+    are checked here, before any kernel could read or write past them."""
+    import torch
     cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
+    lens = np.diff(cu.astype(np.int64))
+    if len(cu) < 2 or cu[0] != 0 or (lens < 0).any() or B <= 0 or H_s <= 0:
+        raise MapFlowError(MF_ERR_ARG, "cu_seqlens must start at 0 and be non-decreasing; "
+                                       "B and H_s positive")
+    nb = (lens + B - 1) // B
+    R = int(nb.sum())
+    C = int((nb * (nb + 1) // 2).sum()) if causal else int((nb * nb).sum())
+    need = (("mass", mass, torch.float32, H_s * C), ("row_ptr", row_ptr, torch.int32, H_s * R + 1),
+            ("col_idx", col_idx, torch.int32, 0), ("nnz", nnz, torch.int64, 1))
+    for name, t, dt, n in need:
+        if t.device.type != "cuda" or t.dtype != dt or not t.is_contiguous():
+            raise MapFlowError(MF_ERR_ARG, f"{name} must be a contiguous CUDA {dt} tensor")
+        if t.numel() < n:
+            raise MapFlowError(MF_ERR_ARG, f"{name} holds {t.numel()} elements, needs {n}")
     _check(load_library().mf_select_noalloc(
         _ptr(mass), cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), len(cu) - 1, H_s, B,
         int(causal), float(p), _ptr(row_ptr), _ptr(col_idx), int(col_idx.numel()), _ptr(nnz),

@@ -427,9 +427,8 @@ MF_API int mf_profile_read(mf_bsr_t h, int kernel, int64_t* launches, double* to
  * caller's block masses, allocating NO device memory.  The pages have no
  * counterpart of this call: it exists for callers that cannot allocate when
  * they select — engines that reserve almost all device memory up front and
- * forbid further cudaMalloc, code inside CUDA stream capture (where
- * cudaMalloc/cudaFree are illegal), and latency-critical loops that cannot
- * pay cudaFree's implicit device synchronisation.
+ * forbid further cudaMalloc, and latency-critical loops that cannot pay
+ * cudaFree's implicit device synchronisation.
  *
  *   mass             fp32 [H_s][C] candidate masses in mf_bsr_export's layout
  *                    (input; e.g. exported from mf_compress)
@@ -449,8 +448,10 @@ MF_API int mf_profile_read(mf_bsr_t h, int kernel, int64_t* launches, double* to
  * stream capture.  All calls on a device share the array: calls that overlap
  * on the GPU (different streams without ordering) race; calls ordered on one
  * stream are safe.  Nothing needs clearing between calls.  The host table of
- * block-rows is copied to the device before the call returns; the kernels
- * run asynchronously on `stream`.
+ * block-rows is copied to the device from a pageable host buffer that the
+ * call owns; such a copy has read the host buffer before cudaMemcpyAsync
+ * returns, so the call frees it on return; the kernels run asynchronously on
+ * `stream`.
  */
 MF_API int mf_select_noalloc(const float* mass, const int32_t* cu_seqlens_host, int n_seqs,
                              int H_s, int B, int causal, float p, int32_t* row_ptr,

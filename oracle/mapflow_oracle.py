@@ -23,7 +23,7 @@ What it follows (the two pages on the method; neither prints pseudo-code):
   multiplied by the receiver's Value and accumulated), and the section on
   reusing token-dependency structure (the receiver keeps its own V).
 
-Readings where the pages are silent (each also listed in the design notes):
+Readings where the pages are silent:
 
 1. Head mapping: A_hat_i = sum_h W[i, h] * A_h of the mapped sender layer,
    W real and signed, no renormalisation; missing blocks count as zero.
@@ -32,7 +32,9 @@ Readings where the pages are silent (each also listed in the design notes):
 3. Selection order: mass descending, ties to the lower block column.  The
    cumulative sum and the threshold are evaluated exactly in fixed point:
    q_b = rint(mass_b * 2**32), Tot = sum q_b, P_q = rint(p * 2**20); keep the
-   shortest sorted prefix with 2**20 * (prefix sum) >= P_q * Tot.
+   shortest sorted prefix with 2**20 * (prefix sum) >= P_q * Tot.  p is the
+   32-bit float the library's entry point receives, so P_q is taken from
+   float32(p), widened exactly.
 4. Causal candidates are the blocks bj <= bi; non-causal: all blocks.
 5. Kept tiles hold the normalised probabilities P_ij, zero above the diagonal
    and outside the sequence; tiles never straddle packed sequences; block
@@ -145,8 +147,10 @@ MASS_FRAC_BITS = 32
 
 
 def threshold_fixed(p: float) -> int:
-    """P_q = rint(p * 2**20) (reading 3)."""
-    return int(np.rint(np.float64(p) * (1 << P_FRAC_BITS)))
+    """P_q = rint(p * 2**20) of the threshold as the compressor receives it:
+    a 32-bit float (reading 3).  float32(p) widens to fp64 exactly and its
+    product with 2**20 is exact, so the only rounding is the rint."""
+    return int(np.rint(np.float64(np.float32(p)) * (1 << P_FRAC_BITS)))
 
 
 def select_topp(mass: Sequence[float], p: float) -> List[int]:
@@ -173,10 +177,6 @@ def select_topp(mass: Sequence[float], p: float) -> List[int]:
         acc += q[order[k]]
         k += 1
     return sorted(order[:k])
-
-
-def select_topp_many(mass_rows: Iterable[Sequence[float]], p: float) -> List[List[int]]:
-    return [select_topp(r, p) for r in mass_rows]
 
 
 # --------------------------------------------------------------------------

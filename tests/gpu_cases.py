@@ -4,8 +4,10 @@ binding on seeded inputs and compare with the fp64 oracle.
 Tolerances:
   * row_ptr / col_idx: bit-exact, with the selection evaluated by the oracle
     on the GPU's own block-mass tensor;
-  * block masses: relative 1e-4 (absolute floor 1e-30, below fp32's normal
-    range);
+  * block masses: relative 1e-4, with an absolute floor of B^2 * 2^-126: the
+    kernels take exp2 with flush-to-zero, so each of a block's B^2
+    probabilities (or a row's partial sum, of which a block has fewer) that
+    falls below fp32's smallest normal 2^-126 may come out as zero;
   * bf16 tiles: within one bf16 ulp of the oracle's probability;
   * row statistics: m within 1e-5 (absolute, natural-log units), l within
     1e-5 relative;
@@ -85,7 +87,7 @@ def check_block_rows(ex, q64, k64, grid: orc.BlockGrid, H_s: int, pairs: Iterabl
         ref = orc.block_row_reference(q64, k64, grid, h, rb)
         got = mass[h, grid.cand_ptr[rb]:grid.cand_ptr[rb + 1]]
         err = np.abs(got - ref["mass"])
-        bad = err > MASS_RTOL * np.abs(ref["mass"]) + 1e-30
+        bad = err > MASS_RTOL * np.abs(ref["mass"]) + grid.B ** 2 * 2.0 ** -126
         assert not bad.any(), f"mass (h={h}, rb={rb}) rel err {np.max(err / np.abs(ref['mass']))}"
         rows = ref["rows"]
         # m_i in fp32 carries three roundings (score, scale to log2 units,

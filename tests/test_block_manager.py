@@ -254,15 +254,47 @@ def test_chunk_rows_equal_the_full_sequence_rows(lib):
     other = np.setdiff1d(np.arange(T), chunk_rows)
     for key in ("row_max", "row_sum"):
         assert np.array_equal(exC[key][:, chunk_rows], exF[key][:, chunk_rows])
+    # the chunk's own rows against the oracle: masses, row statistics and
+    # tiles of every head, and O of every chunk block-row
+    exCg = _chunk_on_full_grid(exC, grid, Hs, rows_f, cand_c)
+    gc.check_block_rows(exCg, x["q64"], x["k64"], grid, Hs,
+                        [(h, rf) for h in range(Hs) for rf in rows_f])
     for Hr, Hkv in ((32, 8), (8, 2)):
-        v = synth.random_v(T, Hkv, 128, 50 + Hkv)["v"][None]
+        vv = synth.random_v(T, Hkv, 128, 50 + Hkv)
+        v = vv["v"][None]
         W = synth.random_w(Hr, Hs, 60 + Hr)[None]
         OF = gc.run_retrieve(F, W, v, Hr, "bf16", [0])[0]
         OC = gc.run_retrieve(Cn, W, v, Hr, "bf16", [0])[0]
         assert np.array_equal(OC[chunk_rows], OF[chunk_rows])
         assert np.isnan(OC[other]).all()
+        gc.check_output(OC, x["q64"], x["k64"], grid, exCg, Hs, W[0].astype(np.float64),
+                        vv["v64"], Hkv, rows_f)
     F.close()
     Cn.close()
+
+
+def _chunk_on_full_grid(exC, grid, Hs, rows_f, cand_c):
+    """A chunked handle's export re-indexed on the full sequence's block grid:
+    the chunk's block-rows keep their masses and kept tiles (the tile indices
+    still point into the chunk's own value buffer, in the same head-major
+    order), every other block-row is empty."""
+    RC = len(rows_f)
+    mass = np.zeros((Hs, grid.C), np.float32)
+    massC = exC["mass"].reshape(Hs, int(cand_c[-1]))
+    rp = np.zeros(Hs * grid.R + 1, np.int64)
+    pos = {rf: j for j, rf in enumerate(rows_f)}
+    nxt = 0
+    for h in range(Hs):
+        for rb in range(grid.R):
+            rp[h * grid.R + rb] = nxt
+            if rb in pos:
+                j = pos[rb]
+                mass[h, grid.cand_ptr[rb]:grid.cand_ptr[rb + 1]] = massC[h, cand_c[j]:cand_c[j + 1]]
+                assert exC["row_ptr"][h * RC + j] == nxt
+                nxt = int(exC["row_ptr"][h * RC + j + 1])
+    rp[-1] = nxt
+    return {"mass": mass.reshape(-1), "row_ptr": rp, "col_idx": exC["col_idx"],
+            "row_max": exC["row_max"], "row_sum": exC["row_sum"], "values_dev": exC["values_dev"]}
 
 
 @pytest.mark.gpu

@@ -233,6 +233,11 @@ def test_retrieve_before_compress_is_rejected():
 # ---------------------------------------------------------------- full size --
 
 def full_size(idx, p=None, sender_layer=None, n_rows=4, receivers=None):
+    """One sender layer of workload idx at its full size: the selection on
+    every row; masses, row statistics and tiles of one random head on the
+    sampled block-rows; and O of every receiver on all the sampled
+    block-rows (block-row 0, the last block-row of every sequence, which is
+    the longest row of its sequence, and n_rows random ones)."""
     w = workloads.get(idx)
     p = w.p[0] if p is None else p
     rcvs = w.receivers if receivers is None else receivers
@@ -255,7 +260,7 @@ def full_size(idx, p=None, sender_layer=None, n_rows=4, receivers=None):
         W = synth.head_map_weights(w, rcv, j)
         O = gc.run_retrieve(bsr, W[None], v["v"][None], rcv.heads, w.dtype, [0])
         res[rcv.name] = gc.check_output(O[0], x["q64"], x["k64"], grid, ex, w.sender_heads, W,
-                                        v["v64"], rcv.kv_heads, rbs[:n_rows])
+                                        v["v64"], rcv.kv_heads, rbs)
         del O
     bsr.close()
     torch.cuda.empty_cache()
@@ -270,7 +275,7 @@ def test_full_workload2():
     full_size(2)
 
 
-@pytest.mark.parametrize("p", [0.80, 0.99])
+@pytest.mark.parametrize("p", [0.80, 0.90, 0.95, 0.99])
 def test_full_workload3(p):
     full_size(3, p=p, n_rows=2)
 
@@ -309,6 +314,14 @@ def test_offload_and_prefetch_roundtrip():
         assert np.array_equal(before[key], after[key]), key
     assert torch.equal(before["values_dev"], after["values_dev"])
     assert np.array_equal(O_before, O_after)
+    # and the layer that came back is the oracle's: structure, masses, row
+    # statistics and tiles of every (head, block-row), O of every block-row
+    grid = orc.BlockGrid(cu, 64, True)
+    gc.check_structure(after, grid, 8, 0.95)
+    gc.check_block_rows(after, x["q64"], x["k64"], grid, 8,
+                        [(h, rb) for h in range(8) for rb in range(grid.R)])
+    gc.check_output(O_after[0], x["q64"], x["k64"], grid, after, 8, W[0].astype(np.float64),
+                    synth.bf16_to_f64(v[0]), 8, range(grid.R))
     assert not np.array_equal(O_other, O_after)
     bsr.offload(0)
     bsr.offload(0)  # a no-op when already offloaded

@@ -174,3 +174,52 @@ def test_map_entries_pin_catches_an_off_by_one_block_mask(monkeypatch):
     monkeypatch.setattr(orc, "kept_mask_rows", shifted_mask)
     with pytest.raises(AssertionError):
         pins.test_map_entries_masks_dropped_blocks_and_rows_sum_to_one()
+
+
+# ------------------------------------------- full-size per-block-row helpers
+
+def _shifted_span(grid, rb):
+    """Row range of a block-row shifted down by one row (a plausible slip in
+    the offset arithmetic), clipped to the sequence."""
+    s, bi = int(grid.rb_seq[rb]), int(grid.rb_local[rb])
+    a, L = int(grid.cu[s]), int(grid.lens[s])
+    r0, r1 = min(L - 1, bi * grid.B + 1), min(L, (bi + 1) * grid.B + 1)
+    return s, bi, a, L, r0, r1
+
+
+def test_helper_pin_catches_an_off_by_one_row_slice_in_block_row_reference(monkeypatch):
+    def shifted(q64, k64, grid, h, rb):
+        Hs, Hks = q64.shape[1], k64.shape[1]
+        s, bi, a, L, r0, r1 = _shifted_span(grid, rb)
+        P, m, l = orc.attention_rows(q64[a + r0:a + r1, h], k64[a:a + L, h // (Hs // Hks)],
+                                     np.arange(r0, r1), grid.causal)
+        return {"P": P, "m": m, "l": l, "mass": orc.block_masses(P, grid.B, int(grid.ncand[rb])),
+                "rows": np.arange(a + r0, a + r1)}
+    monkeypatch.setattr(orc, "block_row_reference", shifted)
+    assert pins.check_block_row_helpers(o=orc) > 1e-3
+
+
+def test_helper_pin_catches_an_off_by_one_row_slice_in_retrieve_block_row(monkeypatch):
+    def shifted(q64, k64, grid, kept_of, W, v64, H_kv, rb):
+        Hs, Hks = q64.shape[1], k64.shape[1]
+        s, bi, a, L, r0, r1 = _shifted_span(grid, rb)
+        Pk = np.zeros((Hs, r1 - r0, L))
+        for h in range(Hs):
+            P, _, _ = orc.attention_rows(q64[a + r0:a + r1, h], k64[a:a + L, h // (Hs // Hks)],
+                                         np.arange(r0, r1), grid.causal)
+            Pk[h] = P * orc.kept_mask_rows(grid, kept_of(h, rb), bi, s, r1 - r0)
+        # the rows reported are the block-row's own, the values are not
+        return orc.retrieve_rows(Pk, W, v64[a:a + L], H_kv), np.arange(a + bi * grid.B,
+                                                                        a + bi * grid.B + r1 - r0)
+    monkeypatch.setattr(orc, "retrieve_block_row", shifted)
+    assert pins.check_block_row_helpers(o=orc) > 1e-3
+
+
+def test_helper_pin_catches_a_wrong_gqa_head_in_block_row_reference(monkeypatch):
+    real = orc.block_row_reference
+
+    def wrong_kv(q64, k64, grid, h, rb):
+        # a wrong sender KV index: the KV heads taken in reverse order
+        return real(q64, k64[:, ::-1], grid, h, rb)
+    monkeypatch.setattr(orc, "block_row_reference", wrong_kv)
+    assert pins.check_block_row_helpers(o=orc) > 1e-3

@@ -166,7 +166,8 @@ def selection_bruteforce(mass, p):
     n = len(mass)
     q = [int(np.rint(x * 2.0 ** 32)) for x in mass]
     tot = sum(q)
-    pq = int(np.rint(p * 2 ** 20))
+    # the threshold as the library receives it: a 32-bit float
+    pq = int(np.rint(float(np.float32(p)) * 2 ** 20))
     for size in range(n + 1):
         ok = [S for S in itertools.combinations(range(n), size)
               if (sum(q[b] for b in S) << 20) >= pq * tot]
@@ -198,6 +199,19 @@ def test_selection_bruteforce(seed):
 def test_selection_fixed_point_constants():
     assert [orc.threshold_fixed(p) for p in (0.80, 0.90, 0.95, 0.99, 1.0)] == \
         [838861, 943718, 996147, 1038090, 1048576]
+
+
+def test_threshold_is_taken_from_the_float32_the_abi_receives():
+    """The compressor's entry point takes p as a 32-bit float, so P_q comes
+    from float32(p).  For p = 838860.51 / 2^20 the double gives
+    rint(838860.51) = 838861, but float32 keeps 24 significant bits (steps of
+    2^-24 here, i.e. 1/16 of a 2^-20 unit), so float32(p) * 2^20 = 838860.5
+    exactly and the half-even rint gives 838860."""
+    p = 838860.51 / 2 ** 20
+    assert float(np.float32(p)) * 2 ** 20 == 838860.5
+    assert orc.threshold_fixed(p) == 838860
+    for x in np.random.default_rng(3).random(200):
+        assert orc.threshold_fixed(float(x)) == orc.threshold_fixed(float(np.float32(x)))
 
 
 def test_selection_uniform_closed_form():
@@ -430,3 +444,72 @@ def test_prefix_block_rows_do_not_depend_on_the_continuation():
                 if not np.allclose(getattr(A, key)[h, :P], getattr(Bq, key)[h, :P], rtol=1e-13):
                     same = False
         assert same == causal
+
+
+# ------------------------------------------- full-size per-block-row helpers
+
+def dense_rows_torch(q, k, cu, h, hk, s, causal):
+    """Scaled logits, their row max and exp-sum, and the softmax of sequence
+    s for one head, all via torch (fp64) over the whole L x L map."""
+    a, b = int(cu[s]), int(cu[s + 1])
+    d = q.shape[2]
+    S = torch.from_numpy(q[a:b, h]) @ torch.from_numpy(k[a:b, hk]).T / math.sqrt(d)
+    if causal:
+        S = S.masked_fill(torch.triu(torch.ones(b - a, b - a, dtype=torch.bool), 1), -math.inf)
+    m = S.max(dim=1).values
+    l = torch.exp(S - m[:, None]).sum(dim=1)
+    return torch.softmax(S, dim=1).numpy(), m.numpy(), l.numpy()
+
+
+def check_block_row_helpers(o=orc, B=16, causal=True, seed=31):
+    """block_row_reference and retrieve_block_row, which the GPU parity tests
+    use at full size one block-row at a time, against (i) whole-sequence
+    softmax maps from torch, sliced at the block-row's rows, and (ii) the
+    oracle's own compress / retrieve.  Packed sequences with ragged tails
+    (and one full-block sequence), a GQA sender (4 q-heads on 2 KV heads) and
+    a receiver with H_r = 6 != H_s on 3 KV groups.  Returns the largest
+    deviation found."""
+    T_list = (45, 70, 2 * B, 33)
+    Hs, Hks, d, Hr, Hkv = 4, 2, 16, 6, 3
+    q, k, cu = rand_case(T_list, Hs, Hks, d, seed)
+    rng = np.random.default_rng(seed + 1)
+    v = rng.standard_normal((sum(T_list), Hkv, d))
+    W = rng.standard_normal((Hr, Hs))
+    bsr = orc.compress(q, k, cu, B, 0.8, causal)
+    O_full, _ = orc.retrieve(q, k, bsr, W, v, Hkv)
+    g = bsr.grid
+    err = 0.0
+    dense = {(h, s): dense_rows_torch(q, k, cu, h, h // (Hs // Hks), s, causal)
+             for h in range(Hs) for s in range(g.n_seqs)}
+    for rb in range(g.R):
+        s, bi = int(g.rb_seq[rb]), int(g.rb_local[rb])
+        a, L = int(cu[s]), int(cu[s + 1] - cu[s])
+        r0, r1 = bi * B, min(L, (bi + 1) * B)
+        want_rows = np.arange(a + r0, a + r1)
+        for h in range(Hs):
+            ref = o.block_row_reference(q, k, g, h, rb)
+            P, m, l = dense[(h, s)]
+            if not np.array_equal(ref["rows"], want_rows) or ref["P"].shape != (r1 - r0, L):
+                return math.inf
+            err = max(err, float(np.abs(ref["P"] - P[r0:r1]).max()),
+                      float(np.abs(ref["m"] - m[r0:r1]).max()),
+                      float(np.abs(ref["l"] / l[r0:r1] - 1).max()))
+            c0, c1 = int(g.cand_ptr[rb]), int(g.cand_ptr[rb + 1])
+            err = max(err, float(np.abs(ref["mass"] - bsr.mass[h, c0:c1]).max()))
+        got, rows = o.retrieve_block_row(q, k, g, bsr.kept, W, v, Hkv, rb)
+        if not np.array_equal(rows, want_rows):
+            return math.inf
+        err = max(err, float(np.abs(got - O_full[want_rows]).max()))
+        # the same rows from the torch maps: sum_h W[i,h] (P_h * kept_h) V_g(i)
+        for i in range(Hr):
+            Ahat = sum(W[i, h] * dense[(h, s)][0][r0:r1] *
+                       orc.kept_mask_rows(g, bsr.kept(h, rb), bi, s, r1 - r0) for h in range(Hs))
+            want = Ahat @ v[a:a + L, i // (Hr // Hkv)]
+            err = max(err, float(np.abs(got[:, i] - want).max()))
+    return err
+
+
+@pytest.mark.parametrize("B", [16, 32])
+@pytest.mark.parametrize("causal", [True, False])
+def test_block_row_helpers(B, causal):
+    assert check_block_row_helpers(B=B, causal=causal) < 1e-13
