@@ -170,3 +170,77 @@ def random_w(Hr: int, Hs: int, seed: int, var: Optional[float] = None) -> np.nda
     rng = np.random.default_rng([seed, 93])
     var = (1.0 / Hs) if var is None else var
     return (rng.standard_normal((Hr, Hs)) * math.sqrt(var)).astype(np.float32)
+
+
+# --------------------------------------------------- device-side drawing ----
+# Full-size benchmark inputs (tens of GB over all layers) would take the host
+# minutes to draw and to hold; these functions draw the same recipe on a CUDA
+# device with torch's generator.  The random numbers differ from the numpy
+# draw above (the distribution and the structure are the same), so parity
+# tests, which compare with the oracle, use the numpy functions.
+
+def _torch_seed(*key: int) -> int:
+    return int(np.random.SeedSequence([int(x) for x in key]).generate_state(1, np.uint64)[0] >> 1)
+
+
+def sender_qk_device(w: Workload, layer: int, device):
+    """Sender Q [T, H_s, d] and K [T, H_ks, d] of sender layer `layer`
+    (1-based), drawn on `device` by the recipe of sender_qk_f32 and rounded
+    once to the workload dtype (torch's fp32 -> bf16 conversion rounds to
+    nearest even)."""
+    import torch
+    d, T = w.d, w.T
+    Hs, Hks = w.sender_heads, w.sender_kv_heads
+    ns = _structure_dims(w)
+    if d < ns + 1:
+        raise ValueError("head dim too small for the structure dims")
+    g = torch.Generator(device=device)
+    g.manual_seed(_torch_seed(w.seed, 11, layer))
+    rng = _rng(w, 11, layer, 1)  # the small per-layer draws (frequencies, blocks, tau)
+    q = torch.zeros((T, Hs, d), dtype=torch.float32, device=device)
+    k = torch.zeros((T, Hks, d), dtype=torch.float32, device=device)
+    q[:, :, ns:] = torch.randn((T, Hs, d - ns), generator=g, device=device) * 1.5
+    k[:, :, ns:] = torch.randn((T, Hks, d - ns), generator=g, device=device) * 1.5
+    sd = math.sqrt(d)
+    omega = torch.from_numpy(rng.uniform(0.0, math.pi / 32.0, size=BAND_PAIRS)).to(device)
+    c = math.sqrt(2.0 / BAND_PAIRS)
+    cu = w.cu_seqlens
+    pos = torch.cat([torch.arange(int(cu[s + 1] - cu[s]), dtype=torch.float64, device=device)
+                     for s in range(len(w.seqlens))])
+    ang = pos[:, None] * omega[None, :]
+    qb = torch.empty((T, 2 * BAND_PAIRS), dtype=torch.float64, device=device)
+    qb[:, 0::2], qb[:, 1::2] = c * torch.cos(ang), c * torch.sin(ang)
+    q[:, :, 1:1 + 2 * BAND_PAIRS] = qb[:, None, :].float()
+    k[:, :, 1:1 + 2 * BAND_PAIRS] = (qb * sd)[:, None, :].float()
+    q[:, :, 0] = 1.0
+    for s in range(len(w.seqlens)):
+        a, b = int(cu[s]), int(cu[s + 1])
+        L = b - a
+        k[a:a + min(SINK_KEYS, L), :, 0] = 4.0 * sd
+        if w.retrieval_blocks:
+            col = 1 + 2 * BAND_PAIRS
+            nb = (L + w.B - 1) // w.B
+            for hk in range(Hks):
+                pick = rng.choice(np.arange(1, nb), size=min(w.retrieval_blocks, nb - 1),
+                                  replace=False)
+                for bj in pick:
+                    k[a + bj * w.B:a + min(L, (bj + 1) * w.B), hk, col] = 3.0 * sd
+    if w.retrieval_blocks:
+        q[:, :, 1 + 2 * BAND_PAIRS] = 1.0
+    if w.temperature is not None:
+        lo, hi = w.temperature
+        tau = torch.from_numpy(rng.uniform(lo, hi, size=Hs).astype(np.float32)).to(device)
+        q /= tau[None, :, None]
+    if w.dtype == "bf16":
+        return q.to(torch.bfloat16), k.to(torch.bfloat16)
+    return q, k
+
+
+def receiver_v_device(w: Workload, rcv: Receiver, layer: int, device):
+    """Receiver V [T, H_kv, d] ~ N(0, 1) of receiver layer j (1-based), drawn
+    on `device`, rounded once to the workload dtype."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(_torch_seed(w.seed, 23, _name_key(rcv.name), layer))
+    v = torch.randn((w.T, rcv.kv_heads, w.d), generator=g, device=device)
+    return v.to(torch.bfloat16) if w.dtype == "bf16" else v
