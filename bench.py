@@ -92,7 +92,8 @@ def traffic_for(kernel: str, alg_bytes: float, max_blocks: int = 0):
 
 def host_budget_bytes() -> int:
     """A share of the host memory this process may still use (the smaller of
-    MemAvailable and the cgroup's remaining limit) for pinned buffers."""
+    MemAvailable and the cgroup's remaining limit), at most 24 GiB, for pinned
+    buffers."""
     avail = None
     try:
         for line in open("/proc/meminfo"):
@@ -108,7 +109,7 @@ def host_budget_bytes() -> int:
             avail = cg if avail is None else min(avail, cg)
     except (OSError, ValueError):
         pass
-    return int(0.35 * (avail if avail is not None else 16 << 30))
+    return int(min(24 << 30, 0.35 * (avail if avail is not None else 16 << 30)))
 
 
 def link_bandwidth(nbytes: int = 256 << 20, reps: int = 4):
@@ -561,7 +562,7 @@ def measure_e2e(mapflow, D, nnz, reps, peaks):
     nnz_e = {l: nnz[D.layers[li[l] % n_h]] for l in D.layers}
     rcvs = w.receivers
     ret_bytes = sum(retrieval_bytes(w, rcvs[ri], nnz_e[m]) for ri, j, m in D.reuse)
-    h2d_b = n_h and sum((D.q[l].numel() + D.k[l].numel()) * 2 for l in D.layers) + \
+    h2d_b = sum((D.q[l].numel() + D.k[l].numel()) * 2 for l in D.layers) + \
         sum(D.v[k].numel() * 2 + D.W[k].numel() * 4 for k in keys)
     d2h_b = sum(D.o[k].numel() * 2 for k in keys)
     # each leg's end-to-end time: the step's end-to-end time minus the other
