@@ -10,8 +10,10 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <map>
 #include <mutex>
 #include <string>
+#include <map>
 #include <vector>
 
 #include "../../include/mapflow.h"
@@ -282,12 +284,49 @@ int mf_bsr_create_chunked(mf_bsr_t* out, int n_layers, int T, int H_s, int B, in
                      const int wa = causal ? a.tl : 0, wb = causal ? b.tl : 0;
                      return wa > wb;
                    });
-  // heaviest slabs first (causal: work grows with the block-row index) so the
-  // tail of the retrieval grid is short
+  // Sequences longest first.  Work that reads a sequence's keys or values
+  // again for every item (the pack's K, the retrieval's V) runs sequence by
+  // sequence, so the items in flight at one time share what they read in L2;
+  // the last items are then the light ones of the shortest sequence.
+  std::vector<int> seq_rank(n_seqs);
+  {
+    std::vector<int> order(n_seqs);
+    for (int s = 0; s < n_seqs; ++s) order[s] = s;
+    std::stable_sort(order.begin(), order.end(), [&](int a, int b) {
+      return h->cu[a + 1] - h->cu[a] > h->cu[b + 1] - h->cu[b];
+    });
+    for (int r = 0; r < n_seqs; ++r) seq_rank[order[r]] = r;
+  }
+  std::map<int, int> rank_of_start;  // sequence start token -> rank
+  for (int s = 0; s < n_seqs; ++s) rank_of_start[h->cu[s]] = seq_rank[s];
+  // heaviest slabs first within each sequence (causal: work grows with the
+  // block-row index) so the tail of the retrieval grid is short
   std::stable_sort(h->slabs.begin(), h->slabs.end(), [&](const RowSlab& a, const RowSlab& b) {
-    const int wa = causal ? h->rbs[a.rb].bi : 0, wb = causal ? h->rbs[b.rb].bi : 0;
+    const RowBlock& ra = h->rbs[a.rb];
+    const RowBlock& rb = h->rbs[b.rb];
+    const int sa = rank_of_start[ra.seq_start], sb = rank_of_start[rb.seq_start];
+    if (sa != sb) return sa < sb;
+    const int wa = causal ? ra.bi : 0, wb = causal ? rb.bi : 0;
     return wa > wb;
   });
+  // The pack's items (tile, head): sequence by sequence, and within a
+  // sequence in chunks of heads whose keys (at most d = 128) fit in 48 MB
+  // of L2, heaviest tiles first within a chunk.  A short sequence is one
+  // chunk, and then the order is the tile-major heavy-first order.
+  if (H_s < 256) {
+    std::vector<std::vector<int>> by_rank(n_seqs);
+    for (int t = 0; t < (int)h->tiles.size(); ++t)
+      by_rank[rank_of_start[h->tiles[t].seq_start]].push_back(t);  // tl descending
+    for (int r = 0; r < n_seqs; ++r) {
+      if (by_rank[r].empty()) continue;
+      const long long L = h->tiles[by_rank[r][0]].L;
+      const long long per_head = L * 128 * 2;
+      const int hc = (int)std::max(1ll, std::min<long long>(H_s, (48ll << 20) / per_head));
+      for (int c0 = 0; c0 < H_s; c0 += hc)
+        for (int t : by_rank[r])
+          for (int hh = c0; hh < std::min(H_s, c0 + hc); ++hh) h->pack_items.push_back(t << 8 | hh);
+    }
+  }
   h->R = (int)h->rbs.size();
   h->C = (int)cand;
   h->n_tiles = (int)h->tiles.size();
@@ -307,6 +346,8 @@ int mf_bsr_create_chunked(mf_bsr_t* out, int n_layers, int T, int H_s, int B, in
   int rc = put((void**)&h->rbs_d, h->rbs.data(), sizeof(RowBlock) * h->rbs.size());
   if (rc == MF_OK) rc = put((void**)&h->tiles_d, h->tiles.data(), sizeof(RowTile) * h->tiles.size());
   if (rc == MF_OK) rc = put((void**)&h->slabs_d, h->slabs.data(), sizeof(RowSlab) * h->slabs.size());
+  if (rc == MF_OK && !h->pack_items.empty())
+    rc = put((void**)&h->pack_items_d, h->pack_items.data(), sizeof(int) * h->pack_items.size());
   if (rc == MF_OK) rc = put((void**)&h->err_d, nullptr, sizeof(int));
   if (rc == MF_OK) {
     cudaError_t e = cudaMemset(h->err_d, 0, sizeof(int));
@@ -338,6 +379,7 @@ void mf_bsr_destroy(mf_bsr_t h) {
   for (auto& L : h->layers) release_layer(h, L, nullptr);
   dev_free(h, h->rbs_d, nullptr);
   dev_free(h, h->tiles_d, nullptr);
+  dev_free(h, h->pack_items_d, nullptr);
   dev_free(h, h->slabs_d, nullptr);
   dev_free(h, h->err_d, nullptr);
   dev_free(h, h->ring, nullptr);
@@ -375,6 +417,7 @@ int mf_compress(mf_bsr_t h, int layer, const void* q, const void* k, int dtype, 
   cp.rbs = h->rbs_d;
   cp.tiles = h->tiles_d;
   cp.n_tiles = h->n_tiles;
+  cp.items = h->pack_items_d;
   cp.T = T;
   cp.H_s = H_s;
   cp.H_ks = H_ks;

@@ -77,6 +77,9 @@ struct mf_bsr_s {
   std::vector<mf::RowSlab> slabs;
   mf::RowBlock* rbs_d = nullptr;
   mf::RowTile* tiles_d = nullptr;
+  // the pack kernel's item order: tile index << 8 | head (sequence-major)
+  std::vector<int> pack_items;
+  int* pack_items_d = nullptr;
   mf::RowSlab* slabs_d = nullptr;
   int* err_d = nullptr;
   long long* host_pinned = nullptr;  // [0] nnz, [1] error word

@@ -34,6 +34,7 @@ struct CompressParams {
   const RowBlock* rbs;
   const RowTile* tiles;
   int n_tiles;
+  const int* items;  // pack order: [n_tiles * H_s] tile index << 8 | head, or null (tile-major)
   int T, H_s, H_ks, d, B, causal;
   int R;            // block-rows
   int C;            // candidates per head

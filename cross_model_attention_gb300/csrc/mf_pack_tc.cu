@@ -153,8 +153,17 @@ __global__ void __launch_bounds__(kPackThreads, (BLK == 64) ? 2 : 1)
         }
         break;
       }
-      // item idx: tile idx / H_s of the heavy-first tile list, head idx % H_s
-      const int ti = idx / p.H_s, h = idx - ti * p.H_s;
+      // item idx: the host's order table, or tile idx / H_s of the
+      // heavy-first tile list and head idx % H_s
+      int ti, h;
+      if (p.items) {
+        const int it = p.items[idx];
+        ti = it >> 8;
+        h = it & 255;
+      } else {
+        ti = idx / p.H_s;
+        h = idx - ti * p.H_s;
+      }
       const RowTile tile = p.tiles[ti];
       const int nsub = kRows / BLK;  // 2 for B=64, 1 for B=128
       int rbv[2], kc[2], base[2];
