@@ -102,20 +102,30 @@ void pin(mf_bm_t bm, BmEntry* e) {
   }
 }
 
-// Evicts least recently used unpinned entries until `need` slots are free;
-// false if the pinned entries leave too few.
-bool make_room(mf_bm_t bm, size_t need, uint64_t protect_from, int64_t* evicted) {
-  while (bm->free_slots.size() < need) {
-    if (bm->lru.empty()) return false;
-    BmEntry* e = bm->lru.begin()->second;
+// The least recently used unpinned entries whose slots, with the free ones,
+// give `need` slots (nothing is changed yet); false if the pinned entries,
+// or those the current call touched, leave too few.
+bool plan_room(mf_bm_t bm, size_t need, uint64_t protect_from, std::vector<BmEntry*>* victims) {
+  size_t have = bm->free_slots.size();
+  for (auto it = bm->lru.begin(); have < need; ++it) {
+    if (it == bm->lru.end()) return false;
+    BmEntry* e = it->second;
     if (e->tick >= protect_from) return false;  // touched by the current call
-    bm->lru.erase(bm->lru.begin());
+    victims->push_back(e);
+    have += e->slots.size();
+  }
+  return true;
+}
+
+// Evicts the planned victims: their slots join the free list.
+void evict(mf_bm_t bm, const std::vector<BmEntry*>& victims, int64_t* evicted) {
+  for (BmEntry* e : victims) {
+    bm->lru.erase({e->tick, e});
     for (int sl : e->slots) bm->free_slots.push_back(sl);
-    bm->index.erase(mf_bm_s::Key{e->key_layer, e->hash});
+    bm->index.erase(mf_bm_s::Key{e->key_layer, e->hash});  // frees e
     ++bm->evictions;
     if (evicted) ++*evicted;
   }
-  return true;
 }
 
 // Copies tile pairs[i].x of `src` into slot pairs[i].y of `dst`, one CTA per
@@ -292,11 +302,21 @@ int mf_bm_insert(mf_bm_t bm, int key_layer, mf_bsr_t h, int layer, const uint64_
     pairs_d = (int2*)pool_alloc(bm, need * sizeof(int2), s);
     if (!pairs_d) return fail(MF_ERR_OOM, "copy list allocation failed");
   }
-  if (!make_room(bm, need, call_tick, &evicted)) {
+  std::vector<BmEntry*> victims;
+  if (!plan_room(bm, need, call_tick, &victims)) {
     pool_free(bm, pairs_d, s);
     return fail(MF_ERR_OOM, "the pool has %zu free tiles for %zu new ones; the rest are pinned or in use by this call",
                 bm->free_slots.size(), need);
   }
+  // the slots the new tiles take: the victims' first, then free ones from the
+  // back of the free list; the victims stay cached until the copy is queued
+  std::vector<int> take;
+  take.reserve(need);
+  for (BmEntry* v : victims)
+    for (int sl : v->slots)
+      if (take.size() < need) take.push_back(sl);
+  const size_t from_free = need - take.size();
+  for (size_t i = 0; i < from_free; ++i) take.push_back(bm->free_slots[bm->free_slots.size() - 1 - i]);
   std::vector<int2> pairs;
   pairs.reserve(need);
   std::vector<std::unique_ptr<BmEntry>> made;
@@ -311,7 +331,7 @@ int mf_bm_insert(mf_bm_t bm, int key_layer, mf_bsr_t h, int layer, const uint64_
     e->where = std::move(nr.where);
     e->slots.resize(e->where.size());
     for (size_t i = 0; i < e->slots.size(); ++i) {
-      e->slots[i] = bm->free_slots[bm->free_slots.size() - 1 - pairs.size()];
+      e->slots[i] = take[pairs.size()];
       pairs.push_back(make_int2(nr.src[i], e->slots[i]));
     }
     made.push_back(std::move(e));
@@ -330,8 +350,20 @@ int mf_bm_insert(mf_bm_t bm, int key_layer, mf_bsr_t h, int layer, const uint64_
     pool_free(bm, pairs_d, s);
     if (e != cudaSuccess) return cuda_fail(e, "tile gather");
   }
-  // commit: the slots leave the free list and the entries enter the index
-  bm->free_slots.resize(bm->free_slots.size() - pairs.size());
+  // commit: the victims leave the cache (their slots not taken return to the
+  // free list), the taken free slots leave it, the new entries enter the index
+  bm->free_slots.resize(bm->free_slots.size() - from_free);
+  {
+    const size_t before = bm->free_slots.size();
+    evict(bm, victims, &evicted);
+    // evict() appended every victim slot; keep only those not taken
+    std::vector<int> rest;
+    size_t skipped = 0;
+    for (size_t i = before; i < bm->free_slots.size(); ++i)
+      if (skipped < need - from_free) ++skipped; else rest.push_back(bm->free_slots[i]);
+    bm->free_slots.resize(before);
+    bm->free_slots.insert(bm->free_slots.end(), rest.begin(), rest.end());
+  }
   for (auto& e : made) {
     e->tick = ++bm->tick;
     bm->lru.insert({e->tick, e.get()});

@@ -40,13 +40,15 @@
 // CTAs walk the same slab list,
 // whose records are staged in shared memory at the start.
 //
-// Warp roles (512 threads): warp 0 TMA loads of V and of the group's A_hat^T,
+// Warp roles (544 threads): warp 0 TMA loads of V and of the group's A_hat^T,
 // warps 11-14 copy sender rows with 16-byte cp.async straight into the
 // swizzled operand layout (their tile indices arrive four blocks ahead),
-// warp 1 issues the combine MMAs, warps 2-9 convert and store A_hat and write
-// each slab's output, warp 10 issues the A_hat.V MMAs, warp 15 publishes
-// stored blocks.  Every wait, on a shared-memory barrier or a global counter,
-// is bounded; the launch is cooperative so a team's CTAs are co-resident.
+// warp 1 issues the combine MMAs, warps 2-9 convert and store A_hat and
+// write each slab's output, warp 10 issues the A_hat.V MMAs, warp 15
+// publishes stored blocks, warp 16 mirrors the team's counters into shared
+// memory.  Every wait, on a shared-memory barrier, a mirror or a global
+// counter, is bounded; the launch is cooperative so a team's CTAs are
+// co-resident.
 #include "mf_internal.cuh"
 #include "mf_ptx.cuh"
 
@@ -54,10 +56,11 @@ namespace mf {
 namespace {
 
 constexpr int kTeam = 8;        // CTAs per team = receiver KV groups
-constexpr int kThreads = 512;   // warp 0 loads, 1 combine MMA, 2-9 convert, 10 A_hat.V MMA, 11-14 P copies, 15 signals
+constexpr int kThreads = 544;   // warp 0 loads, 1 combine MMA, 2-9 convert, 10 A_hat.V MMA, 11-14 P copies, 15 signals, 16 polls
 constexpr int kPThreads = 128;  // P copy threads (warps 11-14)
-constexpr int kPBytes = 96 * 1024;  // P ring: whole blocks of 16-head slices (8 rows x 64 columns, 16 KB)
-constexpr int kSliceBytes = 8 * 16 * 128;
+constexpr int kPBytes = 120 * 1024;  // P ring: whole blocks of head slices (8 rows x 64 columns)
+constexpr int kSliceBytes = 8 * 16 * 128;  // a slice of 16 heads; a last slice of <= 8 heads takes half
+constexpr int kZeroBytes = 2048;           // two zero atoms: the missing head group of a half slice
 constexpr int kPBMax = 3;       // block slots of the P ring at most
 constexpr int kNComb = 32;      // combine N: 8 groups x 4 head slots
 constexpr int kRing = 8;        // global ring slots per team
@@ -65,7 +68,7 @@ constexpr int kASlots = 2;      // A_hat^T tiles staged in shared memory
 constexpr int kSlotHeads = 4;   // head slots per group
 constexpr int kIdxSlots = 8;    // tile-index ring of the copy warps (blocks)
 constexpr int kIdxAhead = 4;    // blocks whose tile indices are requested ahead of the copies
-constexpr int kMaxSlabs = 128;  // slab records of a team kept in shared memory
+constexpr int kMaxSlabs = 32;   // slab records of a team kept in shared memory (later ones from L2)
 constexpr int kGroupElems = kSlotHeads * 64 * 64;  // one group's A_hat in a ring slot
 
 // One slab of a team's list (a 64-row half block-row and its kept columns).
@@ -73,21 +76,29 @@ struct SlabRec {
   int seq_start, L, bi, cand_off, half, n_sub, rb, pad;
 };
 
+// A block slot of the P ring holds the CTA's 8 rows of every sender head in
+// slices of 16 heads, [row 8][head group 2][8 heads][128 B] (row stride 2 KB).
+// When the last slice has at most 8 heads it is stored as [row 8][8 heads]
+// [128 B] (row stride 1 KB), and its MMA descriptor points the missing head
+// group at two shared zero atoms after the ring, so no block slot carries
+// padding: 40 heads take 40 KB and three block slots fit.
 struct TeamLayout {
-  int hpad, nslice, npb, pairs, abuf, vbytes, nv;
-  int off_p, off_a, off_v, off_w, off_s, off_i, off_bar, bytes;
+  int nslice, half_last, slot_bytes, npb, pairs, abuf, vbytes, nv;
+  int off_p, off_zero, off_a, off_v, off_w, off_s, off_i, off_bar, bytes;
   __host__ __device__ TeamLayout(int D, int Hs, int hpc) {
-    hpad = (Hs + 15) / 16 * 16;
-    nslice = hpad / 16;
-    npb = kPBytes / (nslice * kSliceBytes);
+    nslice = (Hs + 15) / 16;
+    half_last = (Hs % 16 != 0 && Hs % 16 <= 8) ? 1 : 0;
+    slot_bytes = nslice * kSliceBytes - (half_last ? kSliceBytes / 2 : 0);
+    npb = kPBytes / slot_bytes;
     if (npb > kPBMax) npb = kPBMax;
     pairs = (hpc + 1) / 2;
     abuf = kGroupElems * 2;
     vbytes = 64 * D * 2;
-    const int base = kPBytes + kASlots * abuf + 4096 + kMaxSlabs * 32 + kIdxSlots * 256;
-    nv = (base + 2 * vbytes + 2048 <= 226 * 1024) ? 2 : 1;
+    const int base = kPBytes + kZeroBytes + kASlots * abuf + 4096 + kMaxSlabs * 32 + kIdxSlots * 256;
+    nv = (base + 2 * vbytes + 1024 + 448 <= 227 * 1024) ? 2 : 1;
     off_p = 0;
-    off_a = off_p + kPBytes;
+    off_zero = off_p + kPBytes;
+    off_a = off_zero + kZeroBytes;
     off_v = off_a + kASlots * abuf;
     off_w = off_v + nv * vbytes;
     off_s = off_w + 4096;
@@ -96,6 +107,12 @@ struct TeamLayout {
     bytes = off_bar + 48 * 8 + 64 + 1024;
   }
 };
+
+// Offset of slice sl within a block slot, and its row stride.
+__device__ __forceinline__ uint32_t slice_off(int sl) { return static_cast<uint32_t>(sl) * kSliceBytes; }
+__device__ __forceinline__ uint32_t slice_row_stride(const TeamLayout& lay, int sl) {
+  return (lay.half_last && sl == lay.nslice - 1) ? 1024u : 2048u;
+}
 
 enum : int {
   kBarVFull = 0, kBarVEmpty = 2, kBarDFull = 4, kBarDEmpty = 6, kBarAFull = 8, kBarAEmpty = 10,
@@ -113,10 +130,45 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int* er
   return ok != 0;
 }
 
-__device__ __forceinline__ bool warp_wait_counter(const uint32_t* ptr, uint32_t target, int* err) {
+// Shared-memory mirrors of the team's ready / freed counters.  The poller
+// warp reads the global counters (one L2 round trip covers all of them) and
+// publishes each change here, so the loader's and the convert warps' per-block
+// waits are shared-memory reads instead of an L2 round trip per block.  The
+// poller's acquire at GPU scope, its release at CTA scope and the waiter's
+// acquire at CTA scope chain the other CTAs' stores before the waiter's
+// later accesses.
+__device__ __forceinline__ uint32_t ld_acquire_cta_shared(const uint32_t* m) {
+  uint32_t v;
+  asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(m)) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_cta_shared(uint32_t* m, uint32_t v) {
+  asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_u32(m)), "r"(v) : "memory");
+}
+// Bounded wait until the mirror reaches `target`; false on timeout (error
+// recorded) or once another role of this CTA has given up.
+__device__ __forceinline__ bool wait_mirror(const uint32_t* m, uint32_t target, int* err,
+                                            volatile int* abort_flag) {
+  if (ld_acquire_cta_shared(m) >= target) return true;
+  const unsigned long long t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (ld_acquire_cta_shared(m) >= target) return true;
+    if ((it & 15u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer() - t0 > kWaitLimitNs) {
+        set_error(err, kDevErrTimeout);
+        return false;
+      }
+    }
+    if (it > 8) __nanosleep(20);
+  }
+}
+__device__ __forceinline__ bool warp_wait_mirror(const uint32_t* m, uint32_t target, int* err,
+                                                 volatile int* abort_flag) {
   int ok = 1;
-  if ((threadIdx.x & 31) == 0) ok = wait_counter(ptr, target, err) ? 1 : 0;
+  if ((threadIdx.x & 31) == 0) ok = wait_mirror(m, target, err, abort_flag) ? 1 : 0;
   ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (ok) (void)ld_acquire_cta_shared(m);
   __syncwarp();
   return ok != 0;
 }
@@ -199,6 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar = [&](int i) { return sb + lay.off_bar + 8u * i; };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + lay.off_bar + kNumBars * 8);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + lay.off_bar + kNumBars * 8 + 16);
+  uint32_t* mirror = reinterpret_cast<uint32_t*>(smem + lay.off_bar + 48 * 8);  // ready[8], freed[8]
   SlabRec* tab = reinterpret_cast<SlabRec*>(smem + lay.off_s);
 
   if (threadIdx.x == 0) {
@@ -219,11 +272,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kRing; ++s) mbar_init(bar(kBarStored + s), 8);
     for (int s = 0; s < kIdxSlots; ++s) mbar_init(bar(kBarIdx + s), kPThreads);
     *abort_flag = 0;
+    for (int i = 0; i < 2 * kRing; ++i) mirror[i] = 0u;  // the counters start each launch at 0
     fence_mbar_init();
   }
   // zero the P ring: the lines of padded heads (beyond H_s in the last
   // slice) are never copied and must hold finite values (their weights are 0)
-  for (int i = threadIdx.x; i < kPBytes / 16; i += kThreads)
+  for (int i = threadIdx.x; i < (kPBytes + kZeroBytes) / 16; i += kThreads)
     *reinterpret_cast<uint4*>(smem + lay.off_p + i * 16) = make_uint4(0u, 0u, 0u, 0u);
   // the team's slab records
   for (int r = threadIdx.x; r < kMaxSlabs; r += kThreads) tab[r] = load_slab<kSub>(r, p, team);
@@ -275,7 +329,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           // this group's A_hat of block u, once all 8 slices are in the slot
           const int as = u % kASlots, s = u % kRing;
           if (!mbar_wait(bar(kBarAEmpty + as), ((u / kASlots) & 1) ^ 1, p.err) ||
-              !wait_counter(ready + s, static_cast<uint32_t>(kTeam * (u / kRing + 1)), p.err)) {
+              !wait_mirror(mirror + s, static_cast<uint32_t>(kTeam * (u / kRing + 1)), p.err,
+                           abort_flag)) {
             ok = false;
             break;
           }
@@ -295,6 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // with the 128-byte swizzle; a dropped or padded head is zero-filled.
     const int t = threadIdx.x - 11 * 32;
     const int hl = t >> 3, cg = t & 7;
+    // (a half slice holds heads hl < 8 only, so its head group is always 0)
     const uint32_t dst0 = sb + lay.off_p + (hl >> 3) * 1024 + sw128_off(hl & 7, cg);
     const size_t row_bytes = static_cast<size_t>(BLK) * 2;
     const char* vbase = reinterpret_cast<const char*>(p.values);
@@ -359,9 +415,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 row_bytes +
                             cs * 128 + cg * 16;
           const uint32_t nbytes = tt >= 0 ? 16u : 0u;  // a dropped head is zero-filled
-          const uint32_t dst = dst0 + (pb * lay.nslice + sl) * kSliceBytes;
+          const uint32_t dst = dst0 + pb * lay.slot_bytes + slice_off(sl);
+          const uint32_t rstride = slice_row_stride(lay, sl);
 #pragma unroll
-          for (int rr = 0; rr < 8; ++rr) cp_async16_hint(dst + rr * 2048, src + rr * row_bytes, nbytes, pol);
+          for (int rr = 0; rr < 8; ++rr) cp_async16_hint(dst + rr * rstride, src + rr * row_bytes, nbytes, pol);
         }
         cp_async_arrive(bar(kBarPFull + pb));
       }
@@ -387,12 +444,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint32_t wbase = sb + lay.off_w;
           for (int sl = 0; sl < lay.nslice; ++sl) {
-            const uint32_t pbase = sb + lay.off_p + (pb * lay.nslice + sl) * kSliceBytes;
+            const uint32_t pbase = sb + lay.off_p + pb * lay.slot_bytes + slice_off(sl);
+            const uint32_t rstride = slice_row_stride(lay, sl);
             const uint64_t bd = sdesc_sw128(wbase + sl * 32, 16, 1024);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-              // rows 2k, 2k+1 of the slice: LBO = row stride (2 KB), SBO = head group (1 KB)
-              const uint64_t ad = sdesc_sw128(pbase + 2 * k * 2048, 2048, 1024);
+              // rows 2k, 2k+1 of the slice: LBO = row stride, SBO = the second
+              // head group (the next atom, or for a half slice the zero atoms)
+              const uint32_t a0 = pbase + 2 * k * rstride;
+              const uint32_t sbo = (rstride == 2048u) ? 1024u : (sb + lay.off_zero) - a0;
+              const uint64_t ad = sdesc_sw128(a0, rstride, sbo);
               tc_mma(tmem + b * 128 + k * kNComb, ad, bd, idesc_comb, sl > 0 ? 1u : 0u);
             }
           }
@@ -449,6 +510,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_commit(bar(kBarO));  // this slab's accumulation is complete
       }
       if (!ok) *abort_flag = 1;
+    }
+  } else if (warp == 16) {
+    // --------------------------------------------------------------- poller
+    // Lane i < 8 follows ready[i], lane 8 + i freed[i]: one acquire load per
+    // lane per round (all in one L2 round trip), each change published to
+    // the shared-memory mirror.  A lane stops once its counter reaches the
+    // value the team's last block gives it, or when the CTA gives up.
+    if (lane < 2 * kRing) {
+      const int sl = lane & (kRing - 1);
+      const uint32_t* src = (lane < kRing ? ready : freed) + sl;
+      int total = 0;
+      for (int r = 0;; ++r) {
+        const SlabRec sr = slab_rec<kSub>(r, tab, p, team);
+        if (sr.n_sub < 0) break;
+        total += sr.n_sub;
+      }
+      const uint32_t final_v =
+          static_cast<uint32_t>(kTeam * (total > sl ? (total - sl + kRing - 1) / kRing : 0));
+      uint32_t last = 0;
+      unsigned long long t0 = globaltimer();
+      while (last < final_v) {
+        const uint32_t v = ld_acquire_gpu(src);
+        if (v != last) {
+          st_release_cta_shared(mirror + lane, v);
+          last = v;
+          t0 = globaltimer();
+          continue;
+        }
+        if (*abort_flag) break;
+        if (globaltimer() - t0 > kWaitLimitNs) {
+          set_error(p.err, kDevErrTimeout);
+          *abort_flag = 1;
+          break;
+        }
+        __nanosleep(32);
+      }
     }
   } else if (warp == 15) {
     // ------------------------------------------------------------ signaller
@@ -511,8 +608,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(bar(kBarDEmpty + b));
         // every owner has its copy of the slot's previous contents
         const int s = u % kRing;
-        if (u >= kRing &&
-            !warp_wait_counter(freed + s, static_cast<uint32_t>(kTeam * (u / kRing)), p.err)) {
+        if (u >= kRing && !warp_wait_mirror(mirror + kRing + s,
+                                            static_cast<uint32_t>(kTeam * (u / kRing)), p.err,
+                                            abort_flag)) {
           ok = false;
           break;
         }

@@ -334,7 +334,9 @@ MF_API int mf_bm_destroy(mf_bm_t bm);
  * `stream`).  counts (optional, HOST int64 [3]): block-rows inserted, found
  * cached, entries evicted.  A hash that names a cached block-row of another
  * position or length is MF_ERR_ARG; more new tiles than the unpinned pool
- * holds is MF_ERR_OOM (nothing is inserted).
+ * holds is MF_ERR_OOM.  A failed insert inserts and evicts nothing (the
+ * entries it would evict leave the cache only once the copy is queued);
+ * cached block-rows it found are still marked used.
  */
 MF_API int mf_bm_insert(mf_bm_t bm, int key_layer, mf_bsr_t h, int layer, const uint64_t* hashes,
                         int64_t* counts, void* stream);
