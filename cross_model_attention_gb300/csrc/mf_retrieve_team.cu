@@ -64,7 +64,8 @@ constexpr int kZeroBytes = 2048;           // two zero atoms: the missing head g
 constexpr int kPBMax = 3;       // block slots of the P ring at most
 constexpr int kNComb = 32;      // combine N: 8 groups x 4 head slots
 constexpr int kRing = 8;        // global ring slots per team
-constexpr int kASlots = 2;      // A_hat^T tiles staged in shared memory
+constexpr int kASub = 4;        // A_hat slots in shared memory: one head pair (2 x 64 rows x 64 keys) each
+constexpr int kPairBytes = 2 * 64 * 64 * 2;
 constexpr int kSlotHeads = 4;   // head slots per group
 constexpr int kIdxSlots = 8;    // tile-index ring of the copy warps (blocks)
 constexpr int kIdxAhead = 4;    // blocks whose tile indices are requested ahead of the copies
@@ -83,7 +84,7 @@ struct SlabRec {
 // group at two shared zero atoms after the ring, so no block slot carries
 // padding: 40 heads take 40 KB and three block slots fit.
 struct TeamLayout {
-  int nslice, half_last, slot_bytes, npb, pairs, abuf, vbytes, nv;
+  int nslice, half_last, slot_bytes, npb, pairs, vbytes, nv;
   int off_p, off_zero, off_a, off_v, off_w, off_s, off_i, off_bar, bytes;
   __host__ __device__ TeamLayout(int D, int Hs, int hpc) {
     nslice = (Hs + 15) / 16;
@@ -92,14 +93,13 @@ struct TeamLayout {
     npb = kPBytes / slot_bytes;
     if (npb > kPBMax) npb = kPBMax;
     pairs = (hpc + 1) / 2;
-    abuf = kGroupElems * 2;
     vbytes = 64 * D * 2;
-    const int base = kPBytes + kZeroBytes + kASlots * abuf + 4096 + kMaxSlabs * 32 + kIdxSlots * 256;
+    const int base = kPBytes + kZeroBytes + kASub * kPairBytes + 4096 + kMaxSlabs * 32 + kIdxSlots * 256;
     nv = (base + 2 * vbytes + 1024 + 448 <= 227 * 1024) ? 2 : 1;
     off_p = 0;
     off_zero = off_p + kPBytes;
     off_a = off_zero + kZeroBytes;
-    off_v = off_a + kASlots * abuf;
+    off_v = off_a + kASub * kPairBytes;
     off_w = off_v + nv * vbytes;
     off_s = off_w + 4096;
     off_i = off_s + kMaxSlabs * 32;
@@ -115,8 +115,9 @@ __device__ __forceinline__ uint32_t slice_row_stride(const TeamLayout& lay, int 
 }
 
 enum : int {
-  kBarVFull = 0, kBarVEmpty = 2, kBarDFull = 4, kBarDEmpty = 6, kBarAFull = 8, kBarAEmpty = 10,
-  kBarO = 12, kBarOFree = 13, kBarStored = 14, kBarPFull = 14 + kRing,
+  kBarVFull = 0, kBarVEmpty = 2, kBarDFull = 4, kBarDEmpty = 6, kBarAFull = 8,
+  kBarAEmpty = kBarAFull + kASub, kBarO = kBarAEmpty + kASub, kBarOFree = kBarO + 1,
+  kBarStored = kBarOFree + 1, kBarPFull = kBarStored + kRing,
   kBarPEmpty = kBarPFull + kPBMax, kBarIdx = kBarPEmpty + kPBMax, kNumBars = kBarIdx + kIdxSlots
 };
 static_assert(kNumBars <= 48, "barrier area");
@@ -264,6 +265,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kBarVEmpty + s), 1);
       mbar_init(bar(kBarDFull + s), 1);
       mbar_init(bar(kBarDEmpty + s), 8);
+    }
+    for (int s = 0; s < kASub; ++s) {
       mbar_init(bar(kBarAFull + s), 1);
       mbar_init(bar(kBarAEmpty + s), 1);
     }
@@ -326,18 +329,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < D / 64; ++c)
             tma_load_2d(sb + lay.off_v + vs * lay.vbytes + c * 8192, &tv, g * D + c * 64, tok0,
                         bar(kBarVFull + vs));
-          // this group's A_hat of block u, once all 8 slices are in the slot
-          const int as = u % kASlots, s = u % kRing;
-          if (!mbar_wait(bar(kBarAEmpty + as), ((u / kASlots) & 1) ^ 1, p.err) ||
-              !wait_mirror(mirror + s, static_cast<uint32_t>(kTeam * (u / kRing + 1)), p.err,
+          // this group's A_hat of block u, once all 8 slices are in the ring
+          // slot, one head pair per shared-memory slot (a pair's slot frees
+          // as soon as its own MMAs are done)
+          const int s = u % kRing;
+          if (!wait_mirror(mirror + s, static_cast<uint32_t>(kTeam * (u / kRing + 1)), p.err,
                            abort_flag)) {
             ok = false;
             break;
           }
           fence_proxy_async_global();
-          mbar_arrive_tx(bar(kBarAFull + as), static_cast<uint32_t>(lay.abuf));
           const int y = ((team * kRing + s) * kTeam + g) * (kGroupElems / 64);
-          tma_load_2d(sb + lay.off_a + as * lay.abuf, &ta, 0, y, bar(kBarAFull + as));
+          for (int pr = 0; pr < lay.pairs; ++pr) {
+            const int q = u * lay.pairs + pr, as = q % kASub;
+            if (!mbar_wait(bar(kBarAEmpty + as), ((q / kASub) & 1) ^ 1, p.err)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_tx(bar(kBarAFull + as), static_cast<uint32_t>(kPairBytes));
+            tma_load_2d(sb + lay.off_a + as * kPairBytes, &ta, 0, y + pr * 128, bar(kBarAFull + as));
+          }
+          if (!ok) break;
         }
       }
       if (!ok) *abort_flag = 1;
@@ -478,33 +490,38 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         for (int j = 0; j < sr.n_sub; ++j, ++u) {
-          const int as = u % kASlots;
           const int vs = (lay.nv == 2) ? (u & 1) : 0;
           const uint32_t vph = (lay.nv == 2) ? ((u >> 1) & 1) : (u & 1);
-          if (!mbar_wait(bar(kBarAFull + as), (u / kASlots) & 1, p.err) ||
-              !mbar_wait(bar(kBarVFull + vs), vph, p.err)) {
+          if (!mbar_wait(bar(kBarVFull + vs), vph, p.err)) {
             ok = false;
             break;
           }
-          // this CTA has its copy of block u's slot (the copy is complete, so
-          // no ordering beyond the count itself is needed)
-          red_relaxed_gpu_add(freed + u % kRing, 1u);
-          tc_fence_after();
-          const uint32_t abase = sb + lay.off_a + as * lay.abuf;
           const uint32_t vbase = sb + lay.off_v + vs * lay.vbytes;
           // O[(head, row), d] += A_hat[(head, row), key] V[key, d], two heads
           // (128 rows of A_hat, K-major) per MMA, 16 keys per step; V is
           // MN-major with d chunks of 64 at 8 KB
           for (int pr = 0; pr < lay.pairs; ++pr) {
+            const int q = u * lay.pairs + pr, as = q % kASub;
+            if (!mbar_wait(bar(kBarAFull + as), (q / kASub) & 1, p.err)) {
+              ok = false;
+              break;
+            }
+            // every pair of block u is in: this CTA has its copy of the ring
+            // slot (the copies are complete, so no ordering beyond the count
+            // itself is needed)
+            if (pr == lay.pairs - 1) red_relaxed_gpu_add(freed + u % kRing, 1u);
+            tc_fence_after();
+            const uint32_t abase = sb + lay.off_a + as * kPairBytes;
 #pragma unroll
             for (int s = 0; s < 4; ++s) {
-              const uint64_t ad = sdesc_sw128(abase + pr * 16384 + s * 32, 16, 1024);
+              const uint64_t ad = sdesc_sw128(abase + s * 32, 16, 1024);
               const uint64_t bd = sdesc_sw128(vbase + s * 2048, 8192, 1024);
               tc_mma(tmem + 256 + pr * D, ad, bd, idesc_av, (j > 0 || s > 0) ? 1u : 0u);
             }
+            tc_commit(bar(kBarAEmpty + as));
           }
+          if (!ok) break;
           tc_commit(bar(kBarVEmpty + vs));
-          tc_commit(bar(kBarAEmpty + as));
         }
         if (!ok) break;
         tc_commit(bar(kBarO));  // this slab's accumulation is complete
@@ -736,7 +753,7 @@ size_t retrieve_team_flag_bytes(int n_teams) {
   return static_cast<size_t>(n_teams) * (2 * kRing + 1) * sizeof(uint32_t);
 }
 
-int retrieve_team_ring_box_rows(int) { return kGroupElems / 64; }
+int retrieve_team_ring_box_rows(int) { return kPairBytes / 128; }
 
 int retrieve_team_ring_rows(int n_teams) { return n_teams * kRing * kTeam * (kGroupElems / 64); }
 
