@@ -8,6 +8,8 @@ counts and mean device times from the library's event profiler, and the kept
 fraction, retrieval GB/s and compressor tokens/s for each top-p value given.
 
     python -m cross_model_attention_gb300.profile_case --workload 1 --layers 2
+    python -m cross_model_attention_gb300.profile_case --workload 3 --layers 1 \
+        --heads 16 --seqlen 16512 --exact --p 0.8      # B = 128 kernels, ~4 GB
 """
 from __future__ import annotations
 
@@ -30,10 +32,21 @@ def main():
     ap.add_argument("--repeat", type=int, default=2)
     ap.add_argument("--p", type=str, default=None,
                     help="top-p, or a comma-separated list: one report per value")
+    ap.add_argument("--heads", type=int, default=None,
+                    help="sender heads (and KV heads), to shrink the device footprint")
+    ap.add_argument("--seqlen", type=int, default=None,
+                    help="one sequence of this length instead of the workload's")
+    ap.add_argument("--exact", action="store_true",
+                    help="size each layer's tiles exactly (one sync) instead of at the bound")
     args = ap.parse_args()
 
     from cross_model_attention_gb300 import accounting, synth, workloads
     w = workloads.get(args.workload)
+    kw = {}
+    if args.heads:
+        kw.update(sender_heads=args.heads, sender_kv_heads=args.heads)
+    if args.seqlen or kw:
+        w = workloads.scaled(w, [args.seqlen] if args.seqlen else w.seqlens, **kw)
     rcv = w.receivers[0]
     lm = rcv.layer_map(w.sender_layers)[:args.layers]
     ps = [w.p[0]] if args.p is None else [float(x) for x in args.p.split(",")]
@@ -55,6 +68,7 @@ def main():
     o = torch.empty((len(lm), w.T, rcv.heads, w.d), dtype=v.dtype, device=dev)
     for p in ps:
         bsr = mapflow.BSR(len(lm), w.T, w.sender_heads, w.B, w.cu_seqlens)
+        bsr.set_exact(args.exact)
         bsr.profile(True)
         for _ in range(args.repeat):
             for l in range(len(lm)):
