@@ -456,6 +456,10 @@ def measure_streamed(mapflow, D, steps, warmup, world, dev, peaks, label, clocks
         "retrieval_binds": "hbm" if roofs["retrieve"]["frac"] >= ret_tensor_frac else "tensor",
         "kept_fraction": float(np.mean([nnz[l] for l in D.layers])) / n_cand,
         "pack_bytes_written_per_step": float(sum(nnz[l] * (2 * w.B * w.B + 4) for l in D.layers)),
+        # the pack recomputes the kept tiles' Q.K^T (reported apart from the
+        # one causal pass the statistics kernel is held to)
+        "pack_recompute_tflops": float(sum(2 * w.d * w.B * w.B * nnz[l] for l in D.layers)) * K
+        / (prof["pack"][1] / 1e3) / 1e12,
         "exp2_per_s": float(sum(L * (L + 1) // 2 for L in w.seqlens)) * w.sender_heads
         * len(D.layers) * K * world / t_comp,
         "rooflines": roofs,
@@ -770,6 +774,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
                            "qk_tflops": roofs["stats"]["achieved"],
                            "exp2_per_s": res["exp2_per_s"],
                            "pack_bytes_written_per_step": res["pack_bytes_written_per_step"],
+                           "pack_recompute_tflops": res["pack_recompute_tflops"],
                            "ms_per_step": res["compressor_ms_per_step"]},
             "retrieval": {"ms_per_step": res["retrieval_ms_per_step"],
                           "bytes_per_step": res["retrieval_bytes_per_step"],
