@@ -580,7 +580,10 @@ def measure_e2e(mapflow, D, nnz, reps, peaks):
             "ms_per_step": 1e3 * statistics.median([s[0] for s in steps]),
             "reps": {"retrieval_gbs": [round(x, 1) for x in ret_gbs],
                      "compressor_tokens_per_s": [round(x) for x in comp_tps],
-                     "ms_per_step": [round(1e3 * s[0], 2) for s in steps]},
+                     "ms_per_step": [round(1e3 * s[0], 2) for s in steps],
+                     # kernel time inside the end-to-end step (per-launch events)
+                     "retrieval_kernel_ms": [round(1e3 * s[1], 2) for s in steps],
+                     "compressor_kernel_ms": [round(1e3 * s[2], 2) for s in steps]},
             "spread": {"retrieval_gbs_min": min(ret_gbs), "retrieval_gbs_max": max(ret_gbs)},
             "link_gbs": links,
             "host_slots": {"qk_layers_distinct": n_h, "v_layers_distinct": n_v,
