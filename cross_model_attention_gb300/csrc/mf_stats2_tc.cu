@@ -13,7 +13,12 @@
 // other's tiles.
 //
 // CTA = persistent walker of (128 query rows of one sequence, one sender head)
-// items.  Warp roles:
+// items, in the handle's order table when it has one: sequence by sequence,
+// heads in chunks whose keys fit in L2, heaviest tiles first within a chunk,
+// so that the CTAs running at one time re-read the same keys from L2 (on 16
+// packed sequences with 40 KV heads this is 4 % faster than the tile-major
+// heavy-first order, which is what a single short sequence gets anyway).
+// Warp roles:
 //   warp 0  TMA producer: Q of each item (one buffer), K tiles of 64 keys
 //           through a 4-6 stage ring that runs on across items
 //   warp 1  tcgen05 issuer: S = Q.K^T (M = 128, N = 64, K = d) into one of
@@ -70,7 +75,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int* er
   return ok != 0;
 }
 
-// Item r of this CTA in a snake order over the heavy-first (tile, head) list:
+// Item r of this CTA in a snake order over the (tile, head) list:
 // round r takes items [r*G, r*G+G), forwards on even rounds and backwards on
 // odd ones, so every CTA's total work stays within one item of the others.
 // -1 once the list is exhausted.
@@ -141,8 +146,9 @@ __global__ void __launch_bounds__(kThreads, 2)
       for (int r = 0; ok; ++r) {
         const int idx = item_of(r, n_items);
         if (idx < 0) break;
-        const RowTile tile = p.tiles[idx / p.H_s];
-        const int h = idx % p.H_s;
+        int ti, h;
+        item_tile_head(p, idx, ti, h);
+        const RowTile tile = p.tiles[ti];
         const int hk = h / (p.H_s / p.H_ks);
         const int n_ct = key_tiles(tile, p.causal);
         // Q of this item replaces the previous item's once its MMAs are done
@@ -181,7 +187,9 @@ __global__ void __launch_bounds__(kThreads, 2)
       for (int r = 0; ok; ++r) {
         const int idx = item_of(r, n_items);
         if (idx < 0) break;
-        const RowTile tile = p.tiles[idx / p.H_s];
+        int ti, hi;
+        item_tile_head(p, idx, ti, hi);
+        const RowTile tile = p.tiles[ti];
         const int n_ct = key_tiles(tile, p.causal);
         if (!mbar_wait(barQFull, r & 1, p.err)) break;
         for (int n = 0; n < n_ct; ++n, ++kt, ++st) {
@@ -219,8 +227,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int r = 0;; ++r) {
       const int idx = item_of(r, n_items);
       if (idx < 0) break;
-      const RowTile tile = p.tiles[idx / p.H_s];
-      const int h = idx % p.H_s;
+      int ti, h;
+      item_tile_head(p, idx, ti, h);
+      const RowTile tile = p.tiles[ti];
       const int n_ct = key_tiles(tile, p.causal);
       const int row_local = tile.tl * kRows + row;
       const bool row_ok = row_local < tile.L;

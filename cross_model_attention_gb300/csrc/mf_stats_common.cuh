@@ -1,12 +1,27 @@
-// mf_stats_common.cuh — helpers shared by the two statistics kernels
-// (mf_stats_tc.cu, mf_stats2_tc.cu): the cross-lane sum of 32 per-lane
-// vectors and the in-place rescale of a warp's TMEM partials.
+// mf_stats_common.cuh — helpers of the statistics kernels (mf_stats_tc.cu,
+// mf_stats2_tc.cu): the item decode of the two-CTA kernel, the cross-lane sum
+// of 32 per-lane vectors and the in-place rescale of a warp's TMEM partials.
 #pragma once
 #include <cstdint>
 
+#include "mf_internal.cuh"
 #include "mf_ptx.cuh"
 
 namespace mf {
+
+// The (128-row tile, head) of item idx: through the handle's order table when
+// there is one (sequence by sequence, heads in chunks whose keys fit in L2,
+// heaviest tiles first within a chunk), else tile-major.
+__device__ __forceinline__ void item_tile_head(const CompressParams& p, int idx, int& ti, int& h) {
+  if (p.items) {
+    const int it = p.items[idx];
+    ti = it >> 8;
+    h = it & 255;
+  } else {
+    ti = idx / p.H_s;
+    h = idx % p.H_s;
+  }
+}
 
 // Sum v[0..31] across the 32 lanes; on return lane l holds the total of
 // element l.  31 shuffles instead of 32*5.
