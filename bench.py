@@ -543,16 +543,23 @@ def measure_e2e(mapflow, D, nnz, reps, peaks):
     torch.cuda.synchronize()
     bsr.device_status()
     steps, links = [], []
+    host_ms = []
     for _ in range(reps):
         link_before = link_bandwidth()
         bsr.profile(True)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(comp)
+        h0 = time.perf_counter()
         issue_copies_in()
+        h1 = time.perf_counter()
         streamed_step(bsr, D, p, waits)
         d2h.wait_stream(comp)
         e1.record(d2h)
+        h2 = time.perf_counter()
         torch.cuda.synchronize()
+        # host time to enqueue the step's input copies and then its kernels and
+        # output copies: milliseconds when the copies are asynchronous
+        host_ms.append((round(1e3 * (h1 - h0), 2), round(1e3 * (h2 - h1), 2)))
         prof = bsr.profile_read()
         t = e0.elapsed_time(e1) / 1e3
         t_ret = prof["retrieve"][1] / 1e3
@@ -586,6 +593,10 @@ def measure_e2e(mapflow, D, nnz, reps, peaks):
                      "compressor_kernel_ms": [round(1e3 * s[2], 2) for s in steps]},
             "spread": {"retrieval_gbs_min": min(ret_gbs), "retrieval_gbs_max": max(ret_gbs)},
             "link_gbs": links,
+            "host_enqueue_ms": {"copies_in": [x[0] for x in host_ms],
+                                "kernels_and_copies_out": [x[1] for x in host_ms]},
+            "host_buffers_pinned": bool(all(t.is_pinned() for t in qh + kh + vh)
+                                        and all(t.is_pinned() for r in oh.values() for t in r)),
             "host_slots": {"qk_layers_distinct": n_h, "v_layers_distinct": n_v,
                            "o_ring": n_o,
                            "note": "step layer i copies host slot i mod n (host memory bound)"},
