@@ -10,6 +10,8 @@ fraction, retrieval GB/s and compressor tokens/s for each top-p value given.
     python -m cross_model_attention_gb300.profile_case --workload 1 --layers 2
     python -m cross_model_attention_gb300.profile_case --workload 3 --layers 1 \
         --heads 16 --seqlen 16512 --exact --p 0.8      # B = 128 kernels, ~4 GB
+    python -m cross_model_attention_gb300.profile_case --workload 1 --layers 2 \
+        --kv-heads 4                                   # the non-team retrieval
 """
 from __future__ import annotations
 
@@ -38,6 +40,8 @@ def main():
                     help="one sequence of this length instead of the workload's")
     ap.add_argument("--exact", action="store_true",
                     help="size each layer's tiles exactly (one sync) instead of at the bound")
+    ap.add_argument("--kv-heads", type=int, default=None,
+                    help="receiver KV heads (other than 8: the non-team retrieval kernel)")
     args = ap.parse_args()
 
     from cross_model_attention_gb300 import accounting, synth, workloads
@@ -48,6 +52,9 @@ def main():
     if args.seqlen or kw:
         w = workloads.scaled(w, [args.seqlen] if args.seqlen else w.seqlens, **kw)
     rcv = w.receivers[0]
+    if args.kv_heads:
+        import dataclasses
+        rcv = dataclasses.replace(rcv, kv_heads=args.kv_heads)
     lm = rcv.layer_map(w.sender_layers)[:args.layers]
     ps = [w.p[0]] if args.p is None else [float(x) for x in args.p.split(",")]
     qk = [synth.sender_qk(w, m) for _, m in lm]
