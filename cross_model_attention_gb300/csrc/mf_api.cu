@@ -309,23 +309,33 @@ int mf_bsr_create_chunked(mf_bsr_t* out, int n_layers, int T, int H_s, int B, in
     const int wa = causal ? ra.bi : 0, wb = causal ? rb.bi : 0;
     return wa > wb;
   });
-  // The pack's items (tile, head): sequence by sequence, and within a
-  // sequence in chunks of heads whose keys (at most d = 128) fit in 48 MB
-  // of L2, heaviest tiles first within a chunk.  A short sequence is one
-  // chunk, and then the order is the tile-major heavy-first order.
+  // The pack's and the two-CTA statistics kernel's items (tile, head):
+  // sequence by sequence, and within a sequence in chunks of heads whose keys
+  // (at most d = 128) fit in a share of L2, heaviest tiles first within a
+  // chunk.  A sequence whose keys fit in 48 MB is one chunk, and then the
+  // order is the tile-major heavy-first order; longer ones are chunked, with
+  // 12 MB of keys per chunk for the pack (its tile stores stream through L2)
+  // and 96 MB for the statistics (measured on 16 packed sequences).
   if (H_s < 256) {
     std::vector<std::vector<int>> by_rank(n_seqs);
     for (int t = 0; t < (int)h->tiles.size(); ++t)
-      by_rank[rank_of_start[h->tiles[t].seq_start]].push_back(t);  // tl descending
-    for (int r = 0; r < n_seqs; ++r) {
-      if (by_rank[r].empty()) continue;
-      const long long L = h->tiles[by_rank[r][0]].L;
-      const long long per_head = L * 128 * 2;
-      const int hc = (int)std::max(1ll, std::min<long long>(H_s, (48ll << 20) / per_head));
-      for (int c0 = 0; c0 < H_s; c0 += hc)
-        for (int t : by_rank[r])
-          for (int hh = c0; hh < std::min(H_s, c0 + hc); ++hh) h->pack_items.push_back(t << 8 | hh);
-    }
+      by_rank[rank_of_start[h->tiles[t].seq_start]].push_back(t);  // tl descending when causal
+    auto build_order = [&](long long chunk_bytes, std::vector<int>& out) {
+      for (int r = 0; r < n_seqs; ++r) {
+        if (by_rank[r].empty()) continue;
+        const long long L = h->tiles[by_rank[r][0]].L;
+        const long long per_head = L * 128 * 2;
+        // a sequence whose keys fit in 48 MB stays one chunk
+        const int hc = per_head * H_s <= (48ll << 20)
+                           ? H_s
+                           : (int)std::max(1ll, std::min<long long>(H_s, chunk_bytes / per_head));
+        for (int c0 = 0; c0 < H_s; c0 += hc)
+          for (int t : by_rank[r])
+            for (int hh = c0; hh < std::min(H_s, c0 + hc); ++hh) out.push_back(t << 8 | hh);
+      }
+    };
+    build_order(12ll << 20, h->pack_items);
+    build_order(96ll << 20, h->stats_items);
   }
   h->R = (int)h->rbs.size();
   h->C = (int)cand;
@@ -348,6 +358,8 @@ int mf_bsr_create_chunked(mf_bsr_t* out, int n_layers, int T, int H_s, int B, in
   if (rc == MF_OK) rc = put((void**)&h->slabs_d, h->slabs.data(), sizeof(RowSlab) * h->slabs.size());
   if (rc == MF_OK && !h->pack_items.empty())
     rc = put((void**)&h->pack_items_d, h->pack_items.data(), sizeof(int) * h->pack_items.size());
+  if (rc == MF_OK && !h->stats_items.empty())
+    rc = put((void**)&h->stats_items_d, h->stats_items.data(), sizeof(int) * h->stats_items.size());
   if (rc == MF_OK) rc = put((void**)&h->err_d, nullptr, sizeof(int));
   if (rc == MF_OK) {
     cudaError_t e = cudaMemset(h->err_d, 0, sizeof(int));
@@ -380,6 +392,7 @@ void mf_bsr_destroy(mf_bsr_t h) {
   dev_free(h, h->rbs_d, nullptr);
   dev_free(h, h->tiles_d, nullptr);
   dev_free(h, h->pack_items_d, nullptr);
+  dev_free(h, h->stats_items_d, nullptr);
   dev_free(h, h->slabs_d, nullptr);
   dev_free(h, h->err_d, nullptr);
   dev_free(h, h->ring, nullptr);
@@ -418,6 +431,7 @@ int mf_compress(mf_bsr_t h, int layer, const void* q, const void* k, int dtype, 
   cp.tiles = h->tiles_d;
   cp.n_tiles = h->n_tiles;
   cp.items = h->pack_items_d;
+  cp.stats_items = h->stats_items_d;
   cp.T = T;
   cp.H_s = H_s;
   cp.H_ks = H_ks;

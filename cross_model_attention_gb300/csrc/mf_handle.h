@@ -80,6 +80,9 @@ struct mf_bsr_s {
   // the pack kernel's item order: tile index << 8 | head (sequence-major)
   std::vector<int> pack_items;
   int* pack_items_d = nullptr;
+  // the two-CTA statistics kernel's item order (same form, larger key chunks)
+  std::vector<int> stats_items;
+  int* stats_items_d = nullptr;
   mf::RowSlab* slabs_d = nullptr;
   int* err_d = nullptr;
   long long* host_pinned = nullptr;  // [0] nnz, [1] error word

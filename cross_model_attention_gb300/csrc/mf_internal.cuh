@@ -35,6 +35,7 @@ struct CompressParams {
   const RowTile* tiles;
   int n_tiles;
   const int* items;  // pack order: [n_tiles * H_s] tile index << 8 | head, or null (tile-major)
+  const int* stats_items;  // the two-CTA statistics kernel's order, same form, or null
   int T, H_s, H_ks, d, B, causal;
   int R;            // block-rows
   int C;            // candidates per head

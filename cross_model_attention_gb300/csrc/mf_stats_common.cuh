@@ -9,12 +9,12 @@
 
 namespace mf {
 
-// The (128-row tile, head) of item idx: through the handle's order table when
-// there is one (sequence by sequence, heads in chunks whose keys fit in L2,
-// heaviest tiles first within a chunk), else tile-major.
+// The (128-row tile, head) of item idx: through the handle's statistics order
+// table when there is one (sequence by sequence, heads in chunks whose keys fit
+// in L2, heaviest tiles first within a chunk), else tile-major.
 __device__ __forceinline__ void item_tile_head(const CompressParams& p, int idx, int& ti, int& h) {
-  if (p.items) {
-    const int it = p.items[idx];
+  if (p.stats_items) {
+    const int it = p.stats_items[idx];
     ti = it >> 8;
     h = it & 255;
   } else {
