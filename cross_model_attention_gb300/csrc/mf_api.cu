@@ -325,10 +325,14 @@ int mf_bsr_create_chunked(mf_bsr_t* out, int n_layers, int T, int H_s, int B, in
         if (by_rank[r].empty()) continue;
         const long long L = h->tiles[by_rank[r][0]].L;
         const long long per_head = L * 128 * 2;
-        // a sequence whose keys fit in 48 MB stays one chunk
-        const int hc = per_head * H_s <= (48ll << 20)
-                           ? H_s
-                           : (int)std::max(1ll, std::min<long long>(H_s, chunk_bytes / per_head));
+        // a sequence whose keys fit in 48 MB stays one chunk; chunks hold a
+        // multiple of 8 query heads when H_s allows, so that no chunk splits
+        // a GQA group of 1, 2, 4 or 8 heads (the handle does not know H_ks;
+        // the byte budget counts every query head's keys, an upper bound)
+        int hc = per_head * H_s <= (48ll << 20)
+                     ? H_s
+                     : (int)std::max(1ll, std::min<long long>(H_s, chunk_bytes / per_head));
+        if (hc < H_s && H_s % 8 == 0) hc = std::min(H_s, (hc + 7) / 8 * 8);
         for (int c0 = 0; c0 < H_s; c0 += hc)
           for (int t : by_rank[r])
             for (int hh = c0; hh < std::min(H_s, c0 + hc); ++hh) out.push_back(t << 8 | hh);
