@@ -469,6 +469,40 @@ def measure_streamed(mapflow, D, steps, warmup, world, dev, peaks, label, clocks
     return res, nnz, U
 
 
+def overlap_probe(torch, bsr, D, p, qhost, comp, h2d):
+    """One input copy (a layer's Q from the leg's own pinned buffer) alone,
+    one layer's compression alone, and both at once on their two streams:
+    where copies and kernels overlap, `both` is near the larger of the two,
+    where they do not, near their sum."""
+    l0 = D.layers[0]
+
+    def run(copy, kernel):
+        e0 = torch.cuda.Event(enable_timing=True)
+        ec = torch.cuda.Event(enable_timing=True)
+        ek = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(comp)
+        h2d.wait_event(e0)
+        if copy:
+            with torch.cuda.stream(h2d):
+                D.q[l0].copy_(qhost, non_blocking=True)
+        ec.record(h2d)
+        if kernel:
+            bsr.compress(0, D.q[l0], D.k[l0], p)
+        ek.record(comp)
+        torch.cuda.synchronize()
+        return max(e0.elapsed_time(ec), e0.elapsed_time(ek))
+
+    run(True, True)
+    t_copy = statistics.median([run(True, False) for _ in range(3)])
+    t_kern = statistics.median([run(False, True) for _ in range(3)])
+    t_both = statistics.median([run(True, True) for _ in range(3)])
+    bsr.release_layer(0)
+    return {"copy_ms": round(t_copy, 3), "copy_gbs": round(qhost.numel() * qhost.element_size()
+                                                          / t_copy / 1e6, 1),
+            "compress_ms": round(t_kern, 3), "both_ms": round(t_both, 3)}
+
+
 def measure_e2e(mapflow, D, nnz, reps, peaks):
     """The same streamed step through the public API with host buffers: every
     step copies each layer's Q/K and each reuse layer's V and W from pinned
@@ -542,6 +576,7 @@ def measure_e2e(mapflow, D, nnz, reps, peaks):
     streamed_step(bsr, D, p, waits)
     torch.cuda.synchronize()
     bsr.device_status()
+    overlap = overlap_probe(torch, bsr, D, p, qh[0], comp, h2d)
     steps, links = [], []
     host_ms = []
     for _ in range(reps):
@@ -595,6 +630,7 @@ def measure_e2e(mapflow, D, nnz, reps, peaks):
             "link_gbs": links,
             "host_enqueue_ms": {"copies_in": [x[0] for x in host_ms],
                                 "kernels_and_copies_out": [x[1] for x in host_ms]},
+            "overlap_probe": overlap,
             "host_buffers_pinned": bool(all(t.is_pinned() for t in qh + kh + vh)
                                         and all(t.is_pinned() for r in oh.values() for t in r)),
             "host_slots": {"qk_layers_distinct": n_h, "v_layers_distinct": n_v,
